@@ -1,0 +1,393 @@
+// Rejection-sampling verification (standard speculative verification:
+// "DSpark" introduction and §2.2; "DSpark: Speculative decodingを活用した…",
+// "問題定義").  Only rows 0..lens[r] of each request are read.
+//
+//  k4_prepare       one CTA: verify-row offsets (exclusive scan of lens + 1),
+//                   clears the rejection list.
+//  k4_target_stats  one warp per (verify row, 1024-column chunk): softmax
+//                   partials of T / temperature (or max / argmax), and the
+//                   target logit at the drafted token.
+//  k4_accept        one warp per request: per row max and normaliser, the
+//                   accept test u < p_t(x) / p_d(x) position by position, the
+//                   bonus draw from row lens[r] when everything is accepted,
+//                   otherwise the request joins the rejection list.
+//  k_vocab_partials<kResidual>  tensor-core recompute of the draft rows at the
+//                   rejected positions fused with max(0, p_t - p_d) partial sums.
+//  k4_residual_sample  one warp per rejected request: inverse CDF of the
+//                   residual (or of p_t when its mass is zero).
+#include <cuda.h>
+
+#include <cmath>
+
+#include "common.h"
+#include "device.cuh"
+#include "vocab_gemm.cuh"
+
+namespace dspark {
+
+struct VerifyArgs {
+  const float* T;          // [R, gamma+1, V]
+  const float* U;          // [R, gamma, V]
+  const uint16_t* W1;
+  const uint16_t* W2;
+  const int32_t* anchors;
+  const int32_t* tokens;   // [R, gamma]
+  const float* pd_tok;     // [R, gamma]
+  const float* logZd;      // [R, gamma]
+  const int32_t* lens;     // [R]
+  int32_t* n_accept;       // [R]
+  int32_t* next_token;     // [R]
+  float2* tstats;          // [R*(gamma+1)][n_vc]
+  float4* trow;            // [R*(gamma+1)]: (max, Z, t(x), -) base-2 units
+  int32_t* rowoff;         // [R+1]
+  int32_t* rej;            // [R_pad + 1]
+  const float2* coarse;    // residual partials [n_chunks][R_pad]
+  const float2* fine;      // [2*n_tiles][R_pad]
+  int32_t* status;
+  int R, R_pad, gamma, V, rank, n_vc, n_tiles, n_chunks;
+  float scale;             // log2(e) / T (1 when greedy)
+  int greedy;
+  uint64_t seed;
+  uint32_t round;
+};
+
+__device__ __forceinline__ int clamp_len(int l, int gamma, int32_t* status) {
+  if (l < 0 || l > gamma) {
+    report(status, DSPARK_STATUS_BAD_LENGTH);
+    return l < 0 ? 0 : gamma;
+  }
+  return l;
+}
+
+__global__ void __launch_bounds__(1024) k4_prepare(const VerifyArgs p) {
+  __shared__ int32_t s_warp[32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int per = (p.R + 1023) / 1024;
+  const int lo = tid * per, hi = min(p.R, lo + per);
+  int run = 0;
+  for (int r = lo; r < hi; ++r) run += clamp_len(p.lens[r], p.gamma, p.status) + 1;
+  int x = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  int off = (x - run) + (wid > 0 ? s_warp[wid - 1] : 0);
+  for (int r = lo; r < hi; ++r) {
+    p.rowoff[r] = off;
+    off += clamp_len(p.lens[r], p.gamma, nullptr) + 1;
+  }
+  if (tid == 1023) p.rowoff[p.R] = s_warp[31];
+  if (tid == 0) p.rej[p.R_pad] = 0;
+}
+
+__global__ void __launch_bounds__(256) k4_target_stats(const VerifyArgs p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int nw = gridDim.x * 8;
+  const int rows = p.rowoff[p.R];
+  const long long items = static_cast<long long>(rows) * p.n_vc;
+  for (long long it = gw; it < items; it += nw) {
+    const int gi = static_cast<int>(it / p.n_vc);
+    const int c = static_cast<int>(it - static_cast<long long>(gi) * p.n_vc);
+    // request owning verify row gi: the last r with rowoff[r] <= gi
+    int lo = 0, hi = p.R - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.rowoff[mid] <= gi) lo = mid; else hi = mid - 1;
+    }
+    const int r = lo, j = gi - p.rowoff[r];
+    const size_t trw = static_cast<size_t>(r) * (p.gamma + 1) + j;
+    const float* row = p.T + trw * p.V;
+    const int c0 = c * kVerifyChunk;
+    const int ncol = min(kVerifyChunk, p.V - c0);
+    float t[32];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int col = (k * 32 + lane) * 4;
+      float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      if (col < ncol) v = __ldcs(reinterpret_cast<const float4*>(row + c0 + col));
+      t[4 * k] = v.x; t[4 * k + 1] = v.y; t[4 * k + 2] = v.z; t[4 * k + 3] = v.w;
+    }
+    float2 res;
+    if (p.greedy) {
+      float mx = -INFINITY;
+      int ix = 0x7fffffff;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int col = c0 + (k >> 2) * 128 + lane * 4 + (k & 3);
+        if (t[k] > mx || (t[k] == mx && col < ix)) { mx = t[k]; ix = col; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, mx, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, ix, o);
+        if (om > mx || (om == mx && oi < ix)) { mx = om; ix = oi; }
+      }
+      res = make_float2(mx, __int_as_float(ix));
+    } else {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) { t[k] *= p.scale; mx = fmaxf(mx, t[k]); }
+      mx = warp_max(mx);
+      float s = 0.f;
+      if (mx > -INFINITY) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s += exp2f(t[k] - mx);
+      }
+      s = warp_sum(s);
+      res = make_float2(mx, s);
+    }
+    if (lane == 0) {
+      p.tstats[trw * p.n_vc + c] = res;
+      if (j < p.gamma) {
+        const int x = p.tokens[static_cast<size_t>(r) * p.gamma + j];
+        if (x >= c0 && x < c0 + ncol) p.trow[trw].z = row[x];
+      }
+    }
+  }
+}
+
+// row max / normaliser from the chunk partials (base-2 units)
+__device__ __forceinline__ void row_stats(const float2* st, int n_vc, float* M_out, double* Z_out) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  for (int c = lane; c < n_vc; c += 32) m = fmaxf(m, st[c].x);
+  const float M = warp_max(m);
+  double z = 0.0;
+  for (int c = lane; c < n_vc; c += 32) {
+    const float2 e = st[c];
+    if (e.x > -INFINITY) z += static_cast<double>(e.y * exp2f(e.x - M));
+  }
+  *M_out = M;
+  *Z_out = warp_sum_d(z);
+}
+__device__ __forceinline__ int row_argmax(const float2* st, int n_vc) {
+  const int lane = threadIdx.x & 31;
+  float best = -INFINITY;
+  int bidx = 0x7fffffff;
+  for (int c = lane; c < n_vc; c += 32) {
+    const float2 e = st[c];
+    const int ei = __float_as_int(e.y);
+    if (e.x > best || (e.x == best && ei < bidx)) { best = e.x; bidx = ei; }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+    if (ob > best || (ob == best && oi < bidx)) { best = ob; bidx = oi; }
+  }
+  return bidx;
+}
+
+// Inverse CDF of softmax(T_row * scale) with target u * Z, via the chunk
+// partials and a scan of the selected 1024-column chunk.
+__device__ int sample_target_row(const VerifyArgs& p, size_t trw, float M, double Z, float u) {
+  const float2* st = p.tstats + trw * p.n_vc;
+  const double target = static_cast<double>(u) * Z;
+  double before = 0.0;
+  const int c = warp_find_crossing(
+      p.n_vc, 0.0, target, [&](int i) -> float { const float2 e = st[i]; return e.x > -INFINITY ? e.y * exp2f(e.x - M) : 0.f; },
+      &before);
+  const float* row = p.T + trw * p.V;
+  const int c0 = c * kVerifyChunk;
+  const int ncol = min(kVerifyChunk, p.V - c0);
+  double b2 = 0.0;
+  const int i = warp_find_crossing(
+      ncol, before, target, [&](int k) -> float { return exp2f(row[c0 + k] * p.scale - M); }, &b2);
+  return c0 + i;
+}
+
+__global__ void __launch_bounds__(128) k4_accept(const VerifyArgs p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (r >= p.R) return;
+  const int len = clamp_len(p.lens[r], p.gamma, nullptr);
+  const size_t base_row = static_cast<size_t>(r) * (p.gamma + 1);
+  if (p.greedy) {
+    int n = len;
+    for (int j = 0; j < len; ++j) {
+      const int am = row_argmax(p.tstats + (base_row + j) * p.n_vc, p.n_vc);
+      if (p.tokens[static_cast<size_t>(r) * p.gamma + j] != am) { n = j; break; }
+    }
+    const int nxt = row_argmax(p.tstats + (base_row + n) * p.n_vc, p.n_vc);
+    if (lane == 0) {
+      p.n_accept[r] = n;
+      p.next_token[r] = (nxt >= 0 && nxt < p.V) ? nxt : 0;
+    }
+    return;
+  }
+  int n = len;
+  float M = 0.f;
+  double Z = 1.0;
+  for (int j = 0; j <= len; ++j) {
+    row_stats(p.tstats + (base_row + j) * p.n_vc, p.n_vc, &M, &Z);
+    if (!(fabsf(M) <= 3.4e38f) || !(Z > 0.0) || !(Z < 1e300)) {
+      if (lane == 0) {
+        report(p.status, DSPARK_STATUS_NONFINITE);
+        p.n_accept[r] = j;
+        p.next_token[r] = 0;
+      }
+      return;
+    }
+    if (lane == 0) p.trow[base_row + j] = make_float4(M, static_cast<float>(Z), p.trow[base_row + j].z, 0.f);
+    if (j == len) break;
+    const float tx = p.trow[base_row + j].z;
+    const double pt = static_cast<double>(exp2f(tx * p.scale - M)) / Z;
+    const float pd = p.pd_tok[static_cast<size_t>(r) * p.gamma + j];
+    const float u = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(j), kAcceptTest);
+    // accept iff u < p_t / p_d, evaluated as u * p_d < p_t (p_d > 0)
+    const bool accept = !(pd > 0.f) || static_cast<double>(u) * static_cast<double>(pd) < pt;
+    if (!accept) { n = j; break; }
+  }
+  const float u2 = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(n), kResidualOrBonus);
+  if (n == len) {
+    const int x = sample_target_row(p, base_row + n, M, Z, u2);
+    if (lane == 0) {
+      p.n_accept[r] = n;
+      p.next_token[r] = min(x, p.V - 1);
+    }
+  } else if (lane == 0) {
+    p.n_accept[r] = n;
+    const int slot = atomicAdd(&p.rej[p.R_pad], 1);
+    p.rej[slot] = r;
+  }
+}
+
+__global__ void __launch_bounds__(128) k4_residual_sample(const VerifyArgs p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (i >= p.rej[p.R_pad]) return;
+  const int r = p.rej[i];
+  const int n = p.n_accept[r];
+  const size_t trw = static_cast<size_t>(r) * (p.gamma + 1) + n;
+  const float4 ts = p.trow[trw];
+  const float Mt = ts.x;
+  const double Zt = static_cast<double>(ts.y);
+  const float u2 = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(n), kResidualOrBonus);
+  const float2* crow = p.coarse + i;
+  double zl = 0.0;
+  for (int c = lane; c < p.n_chunks; c += 32) zl += static_cast<double>(crow[static_cast<size_t>(c) * p.R_pad].x);
+  const double Zr = warp_sum_d(zl);
+  int x;
+  if (!(Zr > 0.0) || !(Zr < 1e300)) {
+    x = sample_target_row(p, trw, Mt, Zt, u2);  // zero residual mass: draw from p_t
+  } else {
+    const double target = static_cast<double>(u2) * Zr;
+    double before_c = 0.0;
+    const int cstar = warp_find_crossing(
+        p.n_chunks, 0.0, target, [&](int c) -> float { return crow[static_cast<size_t>(c) * p.R_pad].x; }, &before_c);
+    const int tb = static_cast<int>((static_cast<long long>(cstar) * p.n_tiles) / p.n_chunks);
+    const int te = static_cast<int>((static_cast<long long>(cstar + 1) * p.n_tiles) / p.n_chunks);
+    const float2* frow = p.fine + i;
+    double before_s = 0.0;
+    const int sstar = 2 * tb + warp_find_crossing(
+                                   2 * (te - tb), before_c, target,
+                                   [&](int k) -> float { return frow[static_cast<size_t>(2 * tb + k) * p.R_pad].x; },
+                                   &before_s);
+    // recompute the 32 residual weights of that sub-tile on CUDA cores
+    const int prev_raw = n == 0 ? p.anchors[r] : p.tokens[static_cast<size_t>(r) * p.gamma + n - 1];
+    const int prev = (prev_raw >= 0 && prev_raw < p.V) ? prev_raw : 0;
+    const float l2zd = p.logZd[static_cast<size_t>(r) * p.gamma + n] * 1.4426950408889634f;
+    const int v = sstar * kSubN + lane;
+    float w = 0.f;
+    if (v < p.V) {
+      const uint16_t* e = p.W1 + static_cast<size_t>(prev) * p.rank;
+      const uint16_t* col = p.W2 + v;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int k = 0; k < p.rank; ++k) acc = fmaf(bf16_at(e + k), bf16_at(col + static_cast<size_t>(k) * p.V), acc);
+      const float pd = exp2f((acc + p.U[(static_cast<size_t>(r) * p.gamma + n) * p.V + v]) * p.scale - l2zd);
+      const float pt = exp2f(p.T[trw * p.V + v] * p.scale - Mt) * static_cast<float>(1.0 / Zt);
+      w = fmaxf(pt - pd, 0.f);
+    }
+    const double incl = before_s + warp_incl_scan_d(static_cast<double>(w));
+    const unsigned cross = __ballot_sync(0xffffffffu, incl > target && w > 0.f);
+    int pick;
+    if (cross) {
+      pick = __ffs(cross) - 1;
+    } else {
+      const unsigned nz = __ballot_sync(0xffffffffu, w > 0.f);
+      pick = nz ? 31 - __clz(nz) : 0;
+    }
+    x = sstar * kSubN + pick;
+  }
+  if (lane == 0) p.next_token[r] = min(max(x, 0), p.V - 1);
+}
+
+int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors,
+                  const int32_t* tokens, const float* pd_tok, const float* logZ, const int32_t* lens, int R, int gamma,
+                  int V, int rank, float temperature, uint64_t seed, uint32_t round, int32_t* n_accept,
+                  int32_t* next_token, void* workspace, cudaStream_t stream) {
+  const WorkspaceLayout L = workspace_layout(R, gamma, V);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  VerifyArgs p = {};
+  p.T = T; p.U = U; p.W1 = W1; p.W2 = W2; p.anchors = anchors; p.tokens = tokens; p.pd_tok = pd_tok;
+  p.logZd = logZ; p.lens = lens; p.n_accept = n_accept; p.next_token = next_token;
+  p.tstats = reinterpret_cast<float2*>(ws + L.tstats);
+  p.trow = reinterpret_cast<float4*>(ws + L.trow);
+  p.rowoff = reinterpret_cast<int32_t*>(ws + L.rowoff);
+  p.rej = reinterpret_cast<int32_t*>(ws + L.rej);
+  p.coarse = reinterpret_cast<const float2*>(ws + L.coarse);
+  p.fine = reinterpret_cast<const float2*>(ws + L.fine);
+  p.status = reinterpret_cast<int32_t*>(ws + L.status);
+  p.R = R; p.gamma = gamma; p.V = V; p.rank = rank;
+  const int n_mtiles = ceil_div(R, kMTile);
+  p.R_pad = n_mtiles * kMTile;
+  p.n_vc = ceil_div(V, kVerifyChunk);
+  p.n_tiles = ceil_div(V, kTileN);
+  p.n_chunks = vocab_chunks(p.n_tiles, n_mtiles);
+  p.greedy = temperature == 0.0f ? 1 : 0;
+  p.scale = p.greedy ? 1.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  p.seed = seed; p.round = round;
+
+  if (launch_pdl(k4_prepare, dim3(1), dim3(1024), 0, stream, true, p) != cudaSuccess) return DSPARK_ERR_CUDA;
+  const long long max_items = static_cast<long long>(R) * (gamma + 1) * p.n_vc;
+  long long blocks = (max_items + 7) / 8;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (launch_pdl(k4_target_stats, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, true, p) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (launch_pdl(k4_accept, dim3(ceil_div(R, 4)), dim3(128), 0, stream, true, p) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (p.greedy) return DSPARK_OK;
+
+  VocabArgs a = {};
+  a.U = U; a.W1 = W1; a.W2 = W2; a.anchors = anchors; a.tokens = tokens;
+  a.coarse = reinterpret_cast<float2*>(ws + L.coarse);
+  a.fine = reinterpret_cast<float2*>(ws + L.fine);
+  a.status = p.status;
+  a.R = R; a.R_pad = p.R_pad; a.gamma = gamma; a.V = V; a.rank = rank; a.step = 0;
+  a.n_tiles = p.n_tiles; a.n_chunks = p.n_chunks; a.n_mtiles = n_mtiles;
+  a.scale = p.scale; a.greedy = 0;
+  a.T = T; a.rej = p.rej; a.n_acc = n_accept; a.trow = p.trow; a.logZd = logZ;
+  CUtensorMap tm;
+  if (encode_w2_map(&tm, W2, V, rank) != DSPARK_OK) return DSPARK_ERR_CUDA;
+  if (launch_vocab_partials(VocabMode::kResidual, tm, a, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (launch_pdl(k4_residual_sample, dim3(ceil_div(R, 4)), dim3(128), 0, stream, true, p) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+}  // namespace dspark

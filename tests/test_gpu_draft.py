@@ -1,0 +1,78 @@
+"""GPU parity of dspark_markov_draft against the CPU oracle."""
+import numpy as np
+import pytest
+
+from gpu_helpers import check_draft, device_round, host, sample_requests
+from semi_autoregressive_speculative_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TINY = synth.WORKLOADS["tiny_r4_g7_v4096"]
+SMALL_CASES = [
+    # (workload, temperatures)
+    (TINY, (1.0, 0.0)),
+    # ragged vocabulary tail (1000 = 15 * 64 + 40), several tiles and chunks
+    (synth.scaled(TINY, R=6, gamma=5, V=1000, d=64, name="ragged_v1000"), (1.0, 0.7, 0.0)),
+    # two M-tiles with a ragged second tile; rank 128
+    (synth.scaled(TINY, R=130, gamma=3, V=2048, rank=128, d=64, name="r130_rank128"), (1.0, 0.0)),
+    # rank 64 and the smallest vocabulary the boundary accepts
+    (synth.scaled(TINY, R=5, gamma=4, V=8, rank=64, d=32, name="v8_rank64"), (1.0, 0.0)),
+    (synth.scaled(TINY, R=3, gamma=6, V=4104, rank=192, d=40, name="v4104_rank192"), (0.7, 0.0)),
+]
+
+
+@pytest.mark.parametrize("wl,temps", SMALL_CASES, ids=lambda x: getattr(x, "name", str(x)))
+def test_draft_small(wl, temps):
+    dr, inp = device_round(wl)
+    for temp in temps:
+        dr.draft(temp, wl.seed, 0)
+        tok, pd, lz = host(dr.tokens), host(dr.pd), host(dr.logZ)
+        assert tok.min() >= 0 and tok.max() < wl.V
+        div, ties = check_draft(wl, inp, tok, pd, lz, temp, 0, range(wl.R))
+        assert div <= max(1, wl.R * wl.gamma // 200)
+        assert ties == 0
+    assert dr.status() == 0
+
+
+def test_draft_zero_markov_head_matches_independent_sampling():
+    # W2 = 0: every position is an independent draw from softmax(U_j / T)
+    wl = synth.scaled(TINY, R=4, gamma=3, V=520, d=16, name="w2zero")
+    dr, inp = device_round(wl)
+    dr.W2.zero_()
+    dr.draft(1.0, 5, 3)
+    tok = host(dr.tokens)
+    import oracle
+    from scipy import special
+    for r in range(wl.R):
+        for j in range(wl.gamma):
+            p = special.softmax(inp.U[r, j].astype(np.float64))
+            u = oracle.uniform(5, 3, r, j, 0)
+            x = int(np.searchsorted(np.cumsum(p), u, side="right"))
+            assert tok[r, j] == x
+
+
+def test_draft_rounds_change_the_draw():
+    wl = synth.scaled(TINY, R=4, gamma=4, V=4096, d=16, name="rounds")
+    dr, _ = device_round(wl)
+    dr.draft(1.0, wl.seed, 0)
+    a = host(dr.tokens).copy()
+    dr.draft(1.0, wl.seed, 1)
+    b = host(dr.tokens)
+    assert (a != b).any()
+    dr.draft(1.0, wl.seed, 0)
+    assert np.array_equal(host(dr.tokens), a)   # deterministic per (seed, round)
+
+
+@pytest.mark.parametrize("name", ["r32_g7_v151936", "r128_g16_v151936", "r512_g16_v32768_staircase",
+                                  "r256_g16_v129280_d7168"])
+def test_draft_full_size_sampled(name):
+    wl = synth.WORKLOADS[name]
+    dr, inp = device_round(wl)
+    for temp in wl.temperatures:
+        dr.draft(temp, wl.seed, 0)
+        tok, pd, lz = host(dr.tokens), host(dr.pd), host(dr.logZ)
+        assert tok.min() >= 0 and tok.max() < wl.V
+        assert np.all(pd > 0) and np.all(pd <= 1.0 + 1e-6) and np.all(np.isfinite(lz))
+        div, ties = check_draft(wl, inp, tok, pd, lz, temp, 0, sample_requests(wl.R))
+        assert div <= 1 and ties == 0
+    assert dr.status() == 0
