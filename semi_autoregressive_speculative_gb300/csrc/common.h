@@ -16,7 +16,8 @@ constexpr int kMTile = 128;        // rows (requests) per tensor-core tile (UMMA
 constexpr int kTileN = 64;         // vocabulary columns per tile (UMMA N)
 constexpr int kSubN = 32;          // columns per fine softmax partial (one epilogue warp)
 constexpr int kMaxChunks = 1024;   // upper bound on contiguous V-chunks per M-tile
-constexpr int kUStride = kTileN * 4 + 16;  // bytes per staged U row (padded: conflict-free)
+constexpr int kUStride = kTileN * 4 + 16;  // bytes per bulk-copied U row (padded: conflict-free)
+constexpr int kPfTiles = 4;        // tiles per L2 prefetch group (a 256-column span per row)
 constexpr int kDraftThreads = 320; // warp 0 TMA producer, warp 1 MMA, warps 2..9 epilogue
 constexpr int kVerifyChunk = 1024; // target columns per verify statistics item
 constexpr int kMaxGamma = 64;
@@ -27,7 +28,7 @@ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 struct WorkspaceLayout {
   size_t status = 0;     // int32 status word (+ padding)
-  size_t coarse = 0;     // float2 [kMaxChunks][R_pad] per-chunk softmax partials
+  size_t coarse = 0;     // float2 [R_pad][kMaxChunks] per-chunk softmax partials
   size_t fine = 0;       // float2 [n_sub][R_pad] per-32-column softmax partials
   size_t tstats = 0;     // float2 [R*(gamma+1)][n_vchunks] target-row partials
   size_t trow = 0;       // float4 [R*(gamma+1)] per target row: (max, sum, t(x), unused)

@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kSchedThreads)
   int32_t* cnt = reinterpret_cast<int32_t*>(sm + plan.cnt);
   double* th = reinterpret_cast<double*>(sm + plan.keys);
   __shared__ int s_red_b[32];
-  __shared__ double s_red_t[32];
+  __shared__ unsigned long long s_red_t[32];
   __shared__ int64_t s_warp[32];
 
   pdl_launch_dependents();
@@ -129,20 +129,27 @@ __global__ void __launch_bounds__(kSchedThreads)
     th[b] = __dmul_rn(tau, sps[R + b]);
   }
   __syncthreads();
-  // first descent (early stop) and global argmax (lowest b on ties)
+  // first descent (early stop) and global argmax (lowest b on ties).  The
+  // comparisons use an order-preserving integer image of each fp64 Theta
+  // (the fp64 pipe of GB300 is slow; the integer compare is exact).
+  auto key = [&](int b) -> unsigned long long {
+    const unsigned long long u = static_cast<unsigned long long>(__double_as_longlong(th[b]));
+    return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+  };
   int my_stop = n;
-  double my_best = -INFINITY;
+  unsigned long long my_best = 0ull;
   int my_arg = 0x7fffffff;
   for (int b = tid; b <= n; b += kSchedThreads) {
-    if (b < n && th[b + 1] <= th[b] && b < my_stop) my_stop = b;
-    if (th[b] > my_best || (th[b] == my_best && b < my_arg)) { my_best = th[b]; my_arg = b; }
+    const unsigned long long kb = key(b);
+    if (b < n && key(b + 1) <= kb && b < my_stop) my_stop = b;
+    if (kb > my_best || (kb == my_best && b < my_arg)) { my_best = kb; my_arg = b; }
   }
   {
     const int lane = tid & 31, wid = tid >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       my_stop = min(my_stop, __shfl_xor_sync(0xffffffffu, my_stop, o));
-      const double ob = __shfl_xor_sync(0xffffffffu, my_best, o);
+      const unsigned long long ob = __shfl_xor_sync(0xffffffffu, my_best, o);
       const int oa = __shfl_xor_sync(0xffffffffu, my_arg, o);
       if (ob > my_best || (ob == my_best && oa < my_arg)) { my_best = ob; my_arg = oa; }
     }
@@ -155,7 +162,7 @@ __global__ void __launch_bounds__(kSchedThreads)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         my_stop = min(my_stop, __shfl_xor_sync(0xffffffffu, my_stop, o));
-        const double ob = __shfl_xor_sync(0xffffffffu, my_best, o);
+        const unsigned long long ob = __shfl_xor_sync(0xffffffffu, my_best, o);
         const int oa = __shfl_xor_sync(0xffffffffu, my_arg, o);
         if (ob > my_best || (ob == my_best && oa < my_arg)) { my_best = ob; my_arg = oa; }
       }

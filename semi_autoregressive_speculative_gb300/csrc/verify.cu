@@ -7,13 +7,13 @@
 //  k4_target_stats  one warp per (verify row, 1024-column chunk): softmax
 //                   partials of T / temperature (or max / argmax), and the
 //                   target logit at the drafted token.
-//  k4_accept        one warp per request: per row max and normaliser, the
+//  k4_accept        one CTA per request: per row max and normaliser, the
 //                   accept test u < p_t(x) / p_d(x) position by position, the
 //                   bonus draw from row lens[r] when everything is accepted,
 //                   otherwise the request joins the rejection list.
 //  k_vocab_partials<kResidual>  tensor-core recompute of the draft rows at the
 //                   rejected positions fused with max(0, p_t - p_d) partial sums.
-//  k4_residual_sample  one warp per rejected request: inverse CDF of the
+//  k4_residual_sample  one CTA per rejected request: inverse CDF of the
 //                   residual (or of p_t when its mass is zero).
 #include <cuda.h>
 
@@ -21,6 +21,7 @@
 
 #include "common.h"
 #include "device.cuh"
+#include "search.cuh"
 #include "vocab_gemm.cuh"
 
 namespace dspark {
@@ -41,7 +42,7 @@ struct VerifyArgs {
   float4* trow;            // [R*(gamma+1)]: (max, Z, t(x), -) base-2 units
   int32_t* rowoff;         // [R+1]
   int32_t* rej;            // [R_pad + 1]
-  const float2* coarse;    // residual partials [n_chunks][R_pad]
+  const float2* coarse;    // residual partials [R_pad][n_chunks]
   const float2* fine;      // [2*n_tiles][R_pad]
   int32_t* status;
   int R, R_pad, gamma, V, rank, n_vc, n_tiles, n_chunks;
@@ -165,18 +166,23 @@ __global__ void __launch_bounds__(256) k4_target_stats(const VerifyArgs p) {
 }
 
 // row max / normaliser from the chunk partials (base-2 units)
-__device__ __forceinline__ void row_stats(const float2* st, int n_vc, float* M_out, double* Z_out) {
+__device__ __forceinline__ void row_stats(const float2* st, int n_vc, float* M_out, float* Z_out) {
   const int lane = threadIdx.x & 31;
-  float m = -INFINITY;
-  for (int c = lane; c < n_vc; c += 32) m = fmaxf(m, st[c].x);
-  const float M = warp_max(m);
-  double z = 0.0;
+  float m = -INFINITY, z = 0.f;  // online (max, sum) per lane, then merged across the warp
   for (int c = lane; c < n_vc; c += 32) {
     const float2 e = st[c];
-    if (e.x > -INFINITY) z += static_cast<double>(e.y * exp2f(e.x - M));
+    if (e.x > -INFINITY) {
+      if (e.x > m) {
+        z = (m > -INFINITY ? z * exp2f(m - e.x) : 0.f) + e.y;
+        m = e.x;
+      } else {
+        z += e.y * exp2f(e.x - m);
+      }
+    }
   }
+  const float M = warp_max(m);
   *M_out = M;
-  *Z_out = warp_sum_d(z);
+  *Z_out = warp_sum(m > -INFINITY ? z * exp2f(m - M) : 0.f);
 }
 __device__ __forceinline__ int row_argmax(const float2* st, int n_vc) {
   const int lane = threadIdx.x & 31;
@@ -198,130 +204,174 @@ __device__ __forceinline__ int row_argmax(const float2* st, int n_vc) {
 
 // Inverse CDF of softmax(T_row * scale) with target u * Z, via the chunk
 // partials and a scan of the selected 1024-column chunk.
-__device__ int sample_target_row(const VerifyArgs& p, size_t trw, float M, double Z, float u) {
+// Block-wide (256 threads); every thread gets the result.
+__device__ int sample_target_row(const VerifyArgs& p, size_t trw, float M, float Z, float u, BlockFindScratch& sc) {
   const float2* st = p.tstats + trw * p.n_vc;
-  const double target = static_cast<double>(u) * Z;
-  double before = 0.0;
-  const int c = warp_find_crossing(
-      p.n_vc, 0.0, target, [&](int i) -> float { const float2 e = st[i]; return e.x > -INFINITY ? e.y * exp2f(e.x - M) : 0.f; },
-      &before);
+  const float target = u * Z;
+  float before = 0.f;
+  const int c = block_find_crossing<256>(
+      p.n_vc, 0.f, target,
+      [&](int i) -> float { const float2 e = st[i]; return e.x > -INFINITY ? e.y * exp2f(e.x - M) : 0.f; }, &before,
+      sc);
   const float* row = p.T + trw * p.V;
   const int c0 = c * kVerifyChunk;
   const int ncol = min(kVerifyChunk, p.V - c0);
-  double b2 = 0.0;
-  const int i = warp_find_crossing(
-      ncol, before, target, [&](int k) -> float { return exp2f(row[c0 + k] * p.scale - M); }, &b2);
+  float b2 = 0.f;
+  const int i = block_find_crossing<256>(
+      ncol, before, target, [&](int k) -> float { return exp2f(row[c0 + k] * p.scale - M); }, &b2, sc);
   return c0 + i;
 }
 
-__global__ void __launch_bounds__(128) k4_accept(const VerifyArgs p) {
+// One CTA per request: warp w computes the statistics of rows w, w+8, ...;
+// the accept tests then run in position order.
+__global__ void __launch_bounds__(256) k4_accept(const VerifyArgs p) {
+  __shared__ BlockFindScratch sc;
+  __shared__ float s_M[kMaxGamma + 1], s_Z[kMaxGamma + 1];
+  __shared__ int s_am[kMaxGamma + 1];
+  __shared__ int s_n;
   pdl_launch_dependents();
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (r >= p.R) return;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int r = blockIdx.x;
   const int len = clamp_len(p.lens[r], p.gamma, nullptr);
   const size_t base_row = static_cast<size_t>(r) * (p.gamma + 1);
-  if (p.greedy) {
+  for (int j = wid; j <= len; j += 8) {
+    const float2* st = p.tstats + (base_row + j) * p.n_vc;
+    if (p.greedy) {
+      const int am = row_argmax(st, p.n_vc);
+      if (lane == 0) s_am[j] = am;
+    } else {
+      float M, Z;
+      row_stats(st, p.n_vc, &M, &Z);
+      if (lane == 0) {
+        s_M[j] = M;
+        s_Z[j] = Z;
+        p.trow[base_row + j] = make_float4(M, Z, p.trow[base_row + j].z, 0.f);
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
     int n = len;
     for (int j = 0; j < len; ++j) {
-      const int am = row_argmax(p.tstats + (base_row + j) * p.n_vc, p.n_vc);
-      if (p.tokens[static_cast<size_t>(r) * p.gamma + j] != am) { n = j; break; }
+      bool accept;
+      if (p.greedy) {
+        accept = p.tokens[static_cast<size_t>(r) * p.gamma + j] == s_am[j];
+      } else {
+        const float M = s_M[j], Z = s_Z[j];
+        if (!(fabsf(M) <= 3.4e38f) || !(Z > 0.f) || !(Z <= 3.4e38f)) {
+          report(p.status, DSPARK_STATUS_NONFINITE);
+          accept = false;
+        } else {
+          const float pt = exp2f(p.trow[base_row + j].z * p.scale - M) / Z;
+          const float pd = p.pd_tok[static_cast<size_t>(r) * p.gamma + j];
+          const float u = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(j), kAcceptTest);
+          // accept iff u < p_t / p_d, evaluated as u * p_d < p_t (p_d > 0)
+          accept = !(pd > 0.f) || u * pd < pt;
+        }
+      }
+      if (!accept) { n = j; break; }
     }
-    const int nxt = row_argmax(p.tstats + (base_row + n) * p.n_vc, p.n_vc);
-    if (lane == 0) {
-      p.n_accept[r] = n;
+    s_n = n;
+    p.n_accept[r] = n;
+  }
+  __syncthreads();
+  const int n = s_n;
+  if (p.greedy) {
+    if (tid == 0) {
+      const int nxt = s_am[n];
       p.next_token[r] = (nxt >= 0 && nxt < p.V) ? nxt : 0;
     }
     return;
   }
-  int n = len;
-  float M = 0.f;
-  double Z = 1.0;
-  for (int j = 0; j <= len; ++j) {
-    row_stats(p.tstats + (base_row + j) * p.n_vc, p.n_vc, &M, &Z);
-    if (!(fabsf(M) <= 3.4e38f) || !(Z > 0.0) || !(Z < 1e300)) {
-      if (lane == 0) {
+  if (n == len) {
+    const float M = s_M[n], Z = s_Z[n];
+    if (!(fabsf(M) <= 3.4e38f) || !(Z > 0.f) || !(Z <= 3.4e38f)) {
+      if (tid == 0) {
         report(p.status, DSPARK_STATUS_NONFINITE);
-        p.n_accept[r] = j;
         p.next_token[r] = 0;
       }
       return;
     }
-    if (lane == 0) p.trow[base_row + j] = make_float4(M, static_cast<float>(Z), p.trow[base_row + j].z, 0.f);
-    if (j == len) break;
-    const float tx = p.trow[base_row + j].z;
-    const double pt = static_cast<double>(exp2f(tx * p.scale - M)) / Z;
-    const float pd = p.pd_tok[static_cast<size_t>(r) * p.gamma + j];
-    const float u = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(j), kAcceptTest);
-    // accept iff u < p_t / p_d, evaluated as u * p_d < p_t (p_d > 0)
-    const bool accept = !(pd > 0.f) || static_cast<double>(u) * static_cast<double>(pd) < pt;
-    if (!accept) { n = j; break; }
-  }
-  const float u2 = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(n), kResidualOrBonus);
-  if (n == len) {
-    const int x = sample_target_row(p, base_row + n, M, Z, u2);
-    if (lane == 0) {
-      p.n_accept[r] = n;
-      p.next_token[r] = min(x, p.V - 1);
-    }
-  } else if (lane == 0) {
-    p.n_accept[r] = n;
+    const float u2 = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(n), kResidualOrBonus);
+    const int x = sample_target_row(p, base_row + n, M, Z, u2, sc);
+    if (tid == 0) p.next_token[r] = min(x, p.V - 1);
+  } else if (tid == 0) {
     const int slot = atomicAdd(&p.rej[p.R_pad], 1);
     p.rej[slot] = r;
   }
 }
 
-__global__ void __launch_bounds__(128) k4_residual_sample(const VerifyArgs p) {
+__global__ void __launch_bounds__(256) k4_residual_sample(const VerifyArgs p) {
+  __shared__ BlockFindScratch sc;
+  __shared__ float s_redz[32];
+  __shared__ float s_e[256];
+  __shared__ float s_part[8][32];
   pdl_launch_dependents();
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int i = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int i = blockIdx.x;
   if (i >= p.rej[p.R_pad]) return;
   const int r = p.rej[i];
   const int n = p.n_accept[r];
   const size_t trw = static_cast<size_t>(r) * (p.gamma + 1) + n;
   const float4 ts = p.trow[trw];
   const float Mt = ts.x;
-  const double Zt = static_cast<double>(ts.y);
+  const float Zt = ts.y;
   const float u2 = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(n), kResidualOrBonus);
-  const float2* crow = p.coarse + i;
-  double zl = 0.0;
-  for (int c = lane; c < p.n_chunks; c += 32) zl += static_cast<double>(crow[static_cast<size_t>(c) * p.R_pad].x);
-  const double Zr = warp_sum_d(zl);
-  int x;
-  if (!(Zr > 0.0) || !(Zr < 1e300)) {
-    x = sample_target_row(p, trw, Mt, Zt, u2);  // zero residual mass: draw from p_t
-  } else {
-    const double target = static_cast<double>(u2) * Zr;
-    double before_c = 0.0;
-    const int cstar = warp_find_crossing(
-        p.n_chunks, 0.0, target, [&](int c) -> float { return crow[static_cast<size_t>(c) * p.R_pad].x; }, &before_c);
-    const int tb = static_cast<int>((static_cast<long long>(cstar) * p.n_tiles) / p.n_chunks);
-    const int te = static_cast<int>((static_cast<long long>(cstar + 1) * p.n_tiles) / p.n_chunks);
-    const float2* frow = p.fine + i;
-    double before_s = 0.0;
-    const int sstar = 2 * tb + warp_find_crossing(
-                                   2 * (te - tb), before_c, target,
-                                   [&](int k) -> float { return frow[static_cast<size_t>(2 * tb + k) * p.R_pad].x; },
-                                   &before_s);
-    // recompute the 32 residual weights of that sub-tile on CUDA cores
-    const int prev_raw = n == 0 ? p.anchors[r] : p.tokens[static_cast<size_t>(r) * p.gamma + n - 1];
-    const int prev = (prev_raw >= 0 && prev_raw < p.V) ? prev_raw : 0;
-    const float l2zd = p.logZd[static_cast<size_t>(r) * p.gamma + n] * 1.4426950408889634f;
-    const int v = sstar * kSubN + lane;
+  const float2* crow = p.coarse + static_cast<size_t>(i) * p.n_chunks;
+  float zl = 0.f;
+  for (int c = tid; c < p.n_chunks; c += 256) zl += crow[c].x;
+  const float Zr = block_sum_f(zl, s_redz);
+  if (!(Zr > 0.f) || !(Zr <= 3.4e38f)) {
+    // zero residual mass: draw from p_t
+    const int x = sample_target_row(p, trw, Mt, Zt, u2, sc);
+    if (tid == 0) p.next_token[r] = min(max(x, 0), p.V - 1);
+    return;
+  }
+  const float target = u2 * Zr;
+  float before_c = 0.f;
+  const int cstar = block_find_crossing<256>(
+      p.n_chunks, 0.f, target, [&](int c) -> float { return crow[c].x; }, &before_c, sc);
+  const int tb = static_cast<int>((static_cast<long long>(cstar) * p.n_tiles) / p.n_chunks);
+  const int te = static_cast<int>((static_cast<long long>(cstar + 1) * p.n_tiles) / p.n_chunks);
+  const float2* frow = p.fine + i;
+  float before_s = 0.f;
+  const int sstar = 2 * tb + block_find_crossing<256>(
+                                 2 * (te - tb), before_c, target,
+                                 [&](int k) -> float { return frow[static_cast<size_t>(2 * tb + k) * p.R_pad].x; },
+                                 &before_s, sc);
+  // recompute the 32 residual weights of that sub-tile: column = lane, rank split over warps
+  const int prev_raw = n == 0 ? p.anchors[r] : p.tokens[static_cast<size_t>(r) * p.gamma + n - 1];
+  const int prev = (prev_raw >= 0 && prev_raw < p.V) ? prev_raw : 0;
+  for (int k = tid; k < p.rank; k += 256) s_e[k] = bf16_at(p.W1 + static_cast<size_t>(prev) * p.rank + k);
+  __syncthreads();
+  const int v = sstar * kSubN + lane;
+  const int per = p.rank / 8;
+  float acc = 0.f;
+  if (v < p.V) {
+    const uint16_t* col = p.W2 + static_cast<size_t>(wid * per) * p.V + v;
+    uint16_t wv[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) wv[k] = k < per ? col[static_cast<size_t>(k) * p.V] : 0;
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (k < per) acc = fmaf(s_e[wid * per + k], __uint_as_float(static_cast<uint32_t>(wv[k]) << 16), acc);
+  }
+  s_part[wid][lane] = acc;
+  __syncthreads();
+  if (wid == 0) {
     float w = 0.f;
     if (v < p.V) {
-      const uint16_t* e = p.W1 + static_cast<size_t>(prev) * p.rank;
-      const uint16_t* col = p.W2 + v;
-      float acc = 0.f;
-#pragma unroll 8
-      for (int k = 0; k < p.rank; ++k) acc = fmaf(bf16_at(e + k), bf16_at(col + static_cast<size_t>(k) * p.V), acc);
-      const float pd = exp2f((acc + p.U[(static_cast<size_t>(r) * p.gamma + n) * p.V + v]) * p.scale - l2zd);
-      const float pt = exp2f(p.T[trw * p.V + v] * p.scale - Mt) * static_cast<float>(1.0 / Zt);
+      float b = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) b += s_part[k][lane];
+      const float l2zd = p.logZd[static_cast<size_t>(r) * p.gamma + n] * 1.4426950408889634f;
+      const float pd = exp2f((b + p.U[(static_cast<size_t>(r) * p.gamma + n) * p.V + v]) * p.scale - l2zd);
+      const float pt = exp2f(p.T[trw * p.V + v] * p.scale - Mt) / Zt;
       w = fmaxf(pt - pd, 0.f);
     }
-    const double incl = before_s + warp_incl_scan_d(static_cast<double>(w));
+    const float incl = before_s + warp_incl_scan_f(w);
     const unsigned cross = __ballot_sync(0xffffffffu, incl > target && w > 0.f);
     int pick;
     if (cross) {
@@ -330,9 +380,8 @@ __global__ void __launch_bounds__(128) k4_residual_sample(const VerifyArgs p) {
       const unsigned nz = __ballot_sync(0xffffffffu, w > 0.f);
       pick = nz ? 31 - __clz(nz) : 0;
     }
-    x = sstar * kSubN + pick;
+    if (lane == 0) p.next_token[r] = min(max(sstar * kSubN + pick, 0), p.V - 1);
   }
-  if (lane == 0) p.next_token[r] = min(max(x, 0), p.V - 1);
 }
 
 int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors,
@@ -369,7 +418,7 @@ int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint
   if (blocks < 1) blocks = 1;
   if (launch_pdl(k4_target_stats, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, true, p) != cudaSuccess)
     return DSPARK_ERR_CUDA;
-  if (launch_pdl(k4_accept, dim3(ceil_div(R, 4)), dim3(128), 0, stream, true, p) != cudaSuccess)
+  if (launch_pdl(k4_accept, dim3(R), dim3(256), 0, stream, true, p) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   if (p.greedy) return DSPARK_OK;
 
@@ -382,10 +431,12 @@ int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint
   a.n_tiles = p.n_tiles; a.n_chunks = p.n_chunks; a.n_mtiles = n_mtiles;
   a.scale = p.scale; a.greedy = 0;
   a.T = T; a.rej = p.rej; a.n_acc = n_accept; a.trow = p.trow; a.logZd = logZ;
-  CUtensorMap tm;
-  if (encode_w2_map(&tm, W2, V, rank) != DSPARK_OK) return DSPARK_ERR_CUDA;
-  if (launch_vocab_partials(VocabMode::kResidual, tm, a, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
-  if (launch_pdl(k4_residual_sample, dim3(ceil_div(R, 4)), dim3(128), 0, stream, true, p) != cudaSuccess)
+  CUtensorMap tm_w2;
+  if (encode_w2_map(&tm_w2, W2, V, rank) != DSPARK_OK) return DSPARK_ERR_CUDA;
+  // the residual pass gathers its U rows with bulk copies: no U tensor map
+  if (launch_vocab_partials(VocabMode::kResidual, tm_w2, tm_w2, a, stream, true) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (launch_pdl(k4_residual_sample, dim3(R), dim3(256), 0, stream, true, p) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }
