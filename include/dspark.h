@@ -48,6 +48,8 @@ extern "C" {
 #define DSPARK_ERR_INVALID_ARG (-1)       /* null pointer, negative size, bad temperature, short workspace, misalignment */
 #define DSPARK_ERR_UNSUPPORTED_SHAPE (-2) /* V % 8 != 0, rank not in {64,128,192,256}, gamma > 64, R*gamma > 8192 (schedule) */
 #define DSPARK_ERR_CUDA (-3)              /* a kernel launch or CUDA runtime call failed */
+#define DSPARK_ERR_STATIC_SCRATCH_TOO_SMALL (-4) /* dspark_markov_draft_noalloc: shape needs more than
+                                                    DSPARK_NOALLOC_SCRATCH_BYTES of scratch */
 
 /* bits of the device status word (first int32 of the workspace) */
 #define DSPARK_STATUS_NONFINITE 1  /* a softmax row had a non-finite max or normaliser */
@@ -155,6 +157,39 @@ int dspark_verify(const float *T, const float *U, const uint16_t *W1, const uint
                   const float *logZ, const int32_t *lens, int R, int gamma, int V, int rank,
                   float temperature, uint64_t seed, uint32_t round, int32_t *n_accept,
                   int32_t *next_token, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * dspark_markov_draft_noalloc — the Markov-head draft of dspark_markov_draft
+ * without a caller workspace.  The pages have no counterpart: this entry point
+ * exists for callers that cannot obtain device memory where they draft, such
+ * as an engine recording its decode step into a CUDA graph (cudaMalloc is not
+ * allowed while capture is open), a serving loop that bans allocator calls
+ * because cudaMalloc / cudaFree can synchronise the device, or a plug-in whose
+ * host program owns all device memory.
+ *
+ * Same inputs, outputs, sizes and results as dspark_markov_draft.  Scratch
+ * (status word and softmax partials) lives in one file-scope device array of
+ * DSPARK_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU loading the library
+ * keeps until the process exits.
+ *   status   int32 [1] or NULL   out: this call's DSPARK_STATUS_* bits (device
+ *                                memory; copied there at the end of the call)
+ * Returns DSPARK_ERR_STATIC_SCRATCH_TOO_SMALL, enqueuing nothing, when the shape
+ * needs more scratch than the array holds: the draft needs 256 B + R_pad * 8 KiB
+ * + R_pad * 16 * ceil(V / 64) bytes with R_pad = R rounded up to 128, e.g.
+ * 5.6 MiB at R = 128, V = 151936 and 9.9 MiB at R = 256, V = 129280.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture begins.  All calls on a device share the
+ * array and it keeps the previous call's contents: each call zeroes the status
+ * word first and rewrites every partial it reads, but calls whose kernels
+ * overlap on the GPU (unordered streams) race on it.  Allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.
+ */
+#define DSPARK_NOALLOC_SCRATCH_BYTES (16u << 20)
+int dspark_markov_draft_noalloc(const float *U, const uint16_t *W1, const uint16_t *W2,
+                                const int32_t *anchors, int R, int gamma, int V, int rank,
+                                float temperature, uint64_t seed, uint32_t round, int32_t *tokens,
+                                float *pd_tok, float *logZ, int32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

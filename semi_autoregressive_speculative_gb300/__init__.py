@@ -17,6 +17,8 @@ DSPARK_OK = 0
 DSPARK_ERR_INVALID_ARG = -1
 DSPARK_ERR_UNSUPPORTED_SHAPE = -2
 DSPARK_ERR_CUDA = -3
+DSPARK_ERR_STATIC_SCRATCH_TOO_SMALL = -4
+DSPARK_NOALLOC_SCRATCH_BYTES = 16 << 20
 DSPARK_STATUS_NONFINITE = 1
 DSPARK_STATUS_BAD_TOKEN = 2
 DSPARK_STATUS_TIMEOUT = 4
@@ -24,14 +26,15 @@ DSPARK_STATUS_BAD_LENGTH = 8
 MODE_EARLY_STOP, MODE_TOP_K, MODE_FIXED = 0, 1, 2
 
 EXPORTS = ("dspark_workspace_size", "dspark_clear_status", "dspark_markov_draft", "dspark_confidence",
-           "dspark_schedule", "dspark_verify")
+           "dspark_schedule", "dspark_verify", "dspark_markov_draft_noalloc")
 
 _lib = None
 
 
 class DsparkError(RuntimeError):
     def __init__(self, fn: str, code: int):
-        names = {-1: "DSPARK_ERR_INVALID_ARG", -2: "DSPARK_ERR_UNSUPPORTED_SHAPE", -3: "DSPARK_ERR_CUDA"}
+        names = {-1: "DSPARK_ERR_INVALID_ARG", -2: "DSPARK_ERR_UNSUPPORTED_SHAPE", -3: "DSPARK_ERR_CUDA",
+                 -4: "DSPARK_ERR_STATIC_SCRATCH_TOO_SMALL"}
         super().__init__(f"{fn} returned {names.get(code, code)}")
         self.code = code
 
@@ -58,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.dspark_schedule.argtypes = [P, I, I, P, I, I, I, P, P, P, P, P, SZ, P]
         L.dspark_verify.restype = I
         L.dspark_verify.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, U64, U32, P, P, P, SZ, P]
+        L.dspark_markov_draft_noalloc.restype = I
+        L.dspark_markov_draft_noalloc.argtypes = [P, P, P, P, I, I, I, I, F, U64, U32, P, P, P, P, P]
         _lib = L
     return _lib
 
@@ -134,3 +139,15 @@ def dspark_verify(T, U, W1, W2, anchors, tokens, pd_tok, logZ, lens, temperature
         _ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _ptr(anchors), _ptr(tokens), _ptr(pd_tok), _ptr(logZ),
         _ptr(lens), R, gamma, V, rank, float(temperature), int(seed), int(round_), _ptr(n_accept),
         _ptr(next_token), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def dspark_markov_draft_noalloc(U, W1, W2, anchors, temperature, seed, round_, tokens, pd_tok, logZ, status=None,
+                                stream=None) -> None:
+    """The draft without a workspace: scratch lives in the library's own
+    16 MiB device array (see include/dspark.h).  `status`, if given, is a
+    device int32 tensor that receives this call's status bits."""
+    R, gamma, V = U.shape
+    rank = W1.shape[1]
+    _check("dspark_markov_draft_noalloc", lib().dspark_markov_draft_noalloc(
+        _ptr(U), _ptr(W1), _ptr(W2), _ptr(anchors), R, gamma, V, rank, float(temperature), int(seed),
+        int(round_), _ptr(tokens), _ptr(pd_tok), _ptr(logZ), _ptr(status), _stream(stream)))
