@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per dspark_markov_draft call (one round's 16 positions) from the
 # ncu capture summarised in profiles/; valid only for the kernel sources
 # whose digest is recorded with it.
-NCU_DRAFT_TRAFFIC = {"digest": None, "bytes_per_call": None}
+NCU_DRAFT_TRAFFIC = {"digest": "fb28b86db73f", "bytes_per_call": 1.93e9 + 51.91e6}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -293,7 +293,8 @@ def run_gpu(args):
         with torch.cuda.graph(g, stream=stream):
             f()
         graphs.append(g)
-    launches_per_step = 2 * wl.gamma + 1 + 1 + (3 if temp == 0 else 5)
+    # draft: one persistent kernel; confidence 1; schedule 1; verify 3 (greedy) or 5
+    launches_per_step = 1 + 1 + 1 + (3 if temp == 0 else 5)
 
     def step(evs=None):
         for i, g in enumerate(graphs):
@@ -395,7 +396,7 @@ def run_gpu(args):
                        "l2": f"inputs larger than L2: U {R * g * V * 4 / 1e9:.2f} GB and T "
                              f"{R * (g + 1) * V * 4 / 1e9:.2f} GB per round",
                        "timing": "4 CUDA graphs per round (draft, confidence, schedule, verify)"},
-            "roofline": {"kernel": "dspark_markov_draft: gamma x (k_vocab_partials<draft> + k1_sample)",
+            "roofline": {"kernel": "k_markov_draft (dspark_markov_draft: one persistent launch, all gamma positions)",
                          "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                          "algorithmic_bytes": draft_bytes, "ms_per_call": per_call[0]},

@@ -23,6 +23,8 @@ constexpr int kVerifyChunk = 1024; // target columns per verify statistics item
 constexpr int kMaxGamma = 64;
 constexpr int kMaxSchedule = 8192; // R * gamma handled by the one-CTA scheduler
 
+constexpr int kMaxSampleChunks = 256; // chunk partials per row the draft sampler holds in registers
+
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -35,6 +37,12 @@ struct WorkspaceLayout {
   size_t rowoff = 0;     // int32 [R+1] verify row offsets
   size_t rej = 0;        // int32 [R_pad] rejecting requests (-1 = none) + count
   size_t total = 0;
+  // The draft's synchronisation words, in the tail of the chunk-partials
+  // region that the draft never uses (it keeps <= kMaxSampleChunks chunks per
+  // row): a done counter and a ready counter per M-tile and the abort word,
+  // each on its own 64-byte line.  Zeroed at the start of every draft call.
+  size_t dsync = 0;
+  size_t dsync_bytes = 0;
 };
 
 inline WorkspaceLayout workspace_layout(int R, int gamma, int V) {
@@ -52,6 +60,8 @@ inline WorkspaceLayout workspace_layout(int R, int gamma, int V) {
   L.rowoff = off; off = align256(off + (static_cast<size_t>(R) + 1) * 4);
   L.rej = off;    off = align256(off + (R_pad + 4) * 4);
   L.total = off;
+  L.dsync = L.coarse + R_pad * kMaxSampleChunks * 8;
+  L.dsync_bytes = 64 * (2 * (R_pad / kMTile) + 1);
   return L;
 }
 

@@ -33,7 +33,7 @@ __device__ __forceinline__ uint64_t philox_word0(uint64_t c0, uint64_t c1, uint6
                                                  uint64_t k0, uint64_t k1) {
   const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
   const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
-#pragma unroll
+#pragma unroll 1  // rolled: the draws sit on latency paths where code size costs more than the loop
   for (int i = 0; i < 10; ++i) {
     const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
     const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;

@@ -1,18 +1,31 @@
 // Markov-head sequential draft ("DSpark" §2.2 eq. p_k, §2.3 eq. B = W1 W2,
-// and the position-by-position loop of §6.2).  Per draft position j:
+// and the position-by-position loop of §6.2) as ONE persistent cooperative
+// kernel per call: every CTA stays resident for all gamma positions.
 //
-//  k_vocab_partials<kDraft> — the tensor-core bias pass of vocab_gemm.cuh:
-//    softmax partials of z_j = (U_j + W1[x_{j-1}] W2) / T per 32-column
-//    sub-tile and per CTA chunk, without writing logits to HBM.
-//  k1_sample — one CTA per request: combines the chunk partials into the
-//    row's max and normaliser, finds the chunk, then the 32-column sub-tile,
-//    in which the cumulative mass first exceeds u * Z, recomputes that
-//    sub-tile's 32 logits on CUDA cores (the rank dimension split over the
-//    CTA's 8 warps) and picks the token; writes x_j, p_d(x_j) and log Z_j.
-//    Greedy: the argmax of the chunk partials.
-//
-// Both kernels and consecutive positions are chained with programmatic
-// dependent launch: the next position's W2 / U loads overlap the sampling.
+// Per position j, on every CTA (one contiguous V-chunk of one 128-row M-tile):
+//   gather   each row's W1[x_{j-1}] goes into tensor memory as the UMMA A
+//            operand, once the sampler that drew x_{j-1} has published it
+//   tiles    W2 tiles (L2-resident after the first position) and U tiles
+//            (one 128-row x 64-column box per tile: 256 contiguous bytes per
+//            row, which is what lets the HBM stream run near its peak) come
+//            in through TMA rings; tcgen05.mma into fp32 accumulators in
+//            tensor memory; the epilogue adds U, scales by log2(e)/T and
+//            reduces each 32-column sub-tile and the whole chunk to softmax
+//            partials (max, sum exp2) — (max, argmax) when greedy.  Logits
+//            never reach HBM.  The CTA then counts itself done on its M-tile.
+//   sample   one warp per request, once every chunk of its M-tile is done:
+//            merges the chunk partials into the row's max and normaliser,
+//            finds the chunk, then the 32-column sub-tile, where the
+//            cumulative mass first exceeds u * Z, recomputes those 32 logits
+//            on CUDA cores, picks x_j, writes x_j, p_d(x_j) and log Z_j and
+//            counts x_j as published on its M-tile.  Greedy: argmax of the
+//            partials.
+// The TMA producer warp never waits for the samplers: W2 and U do not depend
+// on the drafted tokens, so it streams the next position's tiles into the
+// rings while the samplers run.  Every wait is bounded (kWaitLimitNs); a CTA
+// that gives up raises a grid-wide abort word and DSPARK_STATUS_TIMEOUT.
+// Waits are polled by one thread per group (a CTA's gather, a sampler warp)
+// with a short sleep, and shared through named barriers or shuffles.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -23,171 +36,755 @@
 #include "common.h"
 #include "device.cuh"
 #include "search.cuh"
-#include "vocab_gemm.cuh"
+#include "vocab_common.h"
 
 namespace dspark {
 
-constexpr int kSampleThreads = 256;
+constexpr int kDraftWStages = 3;  // W2 tiles in flight per CTA (L2-resident after the first position)
+constexpr int kDraftUStages = 3;  // U tiles in flight per CTA (the HBM stream)
+// A U tile is one 128-row x 68-column box: the 64 columns of the tile plus the
+// first 4 of the next.  Each request row is one 272-byte run in HBM (runs of
+// 256 bytes and more keep the stream near the copy rate; 128-byte runs lose
+// about a third of it), and the 272-byte row pitch in shared memory puts 8
+// consecutive rows on 8 different bank groups, so the epilogue's 16-byte reads
+// are conflict-free.
+constexpr int kDraftUCols = kTileN + 4;
+constexpr int kDraftUBytes = kMTile * kDraftUCols * 4;
+constexpr int kEpiThreads = kDraftThreads - 64;  // warps 2..9
+constexpr int kMaxDraftV = 1 << 24;               // vocabulary bound of the 32-bit chunk arithmetic
 
-struct SampleArgs {
-  const float* U;
-  const uint16_t* W1;
-  const uint16_t* W2;
-  const int32_t* anchors;
-  int32_t* tokens;
-  float* pd_tok;
-  float* logZ;
-  const float2* coarse;  // [R_pad][n_chunks]
-  const float2* fine;    // [2 * n_tiles][R_pad]
+struct DraftArgs {
+  const float* U;          // [R, gamma, V]
+  const uint16_t* W1;      // [V, rank]
+  const uint16_t* W2;      // [rank, V]
+  const int32_t* anchors;  // [R]
+  int32_t* tokens;         // [R, gamma]
+  float* pd_tok;           // [R, gamma]
+  float* logZ;             // [R, gamma]
+  float2* coarse;          // [R_pad][n_chunks]
+  float2* fine;            // [2 * n_tiles][R_pad]
   int32_t* status;
-  int R, R_pad, gamma, V, rank, step, n_tiles, n_chunks;
-  float scale;
-  int greedy;
+  uint32_t* done;          // [n_mtiles] CTAs that finished a position, 16 words apart
+  uint32_t* ready;         // [n_mtiles] tokens published, 16 words apart
+  uint32_t* abort;         // any CTA gave up on a wait
+  int R, R_pad, gamma, V, rank, n_tiles, n_chunks, n_mtiles;
+  float scale;             // log2(e) / T (1 when greedy)
   uint64_t seed;
   uint32_t round;
 };
 
-__global__ void __launch_bounds__(kSampleThreads) k1_sample(const SampleArgs p) {
-  __shared__ BlockFindScratch sc;
-  __shared__ float s_redf[32];
-  __shared__ float s_redz[32];
-  __shared__ int s_redi[32];
-  __shared__ float s_e[256];
-  __shared__ float s_part[kSampleThreads / 32][32];
-  pdl_launch_dependents();
-  pdl_wait();
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int r = blockIdx.x;
-  const size_t out = static_cast<size_t>(r) * p.gamma + p.step;
-  const float2* crow = p.coarse + static_cast<size_t>(r) * p.n_chunks;
+struct DraftSmem {
+  uint32_t w[kDraftWStages], u[kDraftUStages], half, bars, slots, part, wts, slab, total;
+};
+__host__ __device__ inline DraftSmem draft_smem_plan(int rank) {
+  DraftSmem s;
+  uint32_t off = 0;
+  for (int i = 0; i < kDraftWStages; ++i) { s.w[i] = off; off += 128u * rank; }  // rank x 64 bf16, SW128
+  for (int i = 0; i < kDraftUStages; ++i) { s.u[i] = off; off += kDraftUBytes; }
+  s.half = off; off += kMTile * 8;
+  s.bars = off; off += 256;
+  s.slots = off; off += 32;                      // the sampler's SampleSlot
+  s.part = off; off += 8 * 32 * 4;               // each epilogue warp's 32 column shares
+  s.wts = off; off += kMaxSampleChunks * 4;      // the leader's search weights
+  off = (off + 127u) & ~127u;
+  s.slab = off; off += 64u * rank + 32 * 4;      // W2 columns [rank][32] bf16, then 32 U values
+  s.total = off + 1024;  // alignment slack
+  return s;
+}
 
-  if (p.greedy) {
-    float best = -INFINITY;
-    int bidx = 0x7fffffff;
-    for (int c = tid; c < p.n_chunks; c += kSampleThreads) {
-      const float2 e = crow[c];
-      const int ei = __float_as_int(e.y);
-      if (e.x > best || (e.x == best && ei < bidx)) { best = e.x; bidx = ei; }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-      if (ob > best || (ob == best && oi < bidx)) { best = ob; bidx = oi; }
-    }
-    if (lane == 0) { s_redf[wid] = best; s_redi[wid] = bidx; }
-    __syncthreads();
-    if (wid == 0) {
-      best = lane < kSampleThreads / 32 ? s_redf[lane] : -INFINITY;
-      bidx = lane < kSampleThreads / 32 ? s_redi[lane] : 0x7fffffff;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-        if (ob > best || (ob == best && oi < bidx)) { best = ob; bidx = oi; }
-      }
-      if (lane == 0) {
-        if (!(fabsf(best) <= 3.4e38f) || bidx < 0 || bidx >= p.V) {
-          report(p.status, DSPARK_STATUS_NONFINITE);
-          bidx = 0;
-        }
-        p.tokens[out] = bidx;
-        p.pd_tok[out] = 1.0f;
-        p.logZ[out] = best;
-      }
-    }
-    return;
-  }
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+// 2^x on the SFU (ex2.approx.ftz; results below 2^-126 flush to 0, which
+// changes no softmax sum at the fp32 precision the partials carry).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
-  // the previous token's W1 row, needed by the recompute at the end
-  const int prev_raw = p.step == 0 ? p.anchors[r] : p.tokens[static_cast<size_t>(r) * p.gamma + p.step - 1];
-  const int prev = (prev_raw >= 0 && prev_raw < p.V) ? prev_raw : 0;
-  for (int i = tid; i < p.rank; i += kSampleThreads) s_e[i] = bf16_at(p.W1 + static_cast<size_t>(prev) * p.rank + i);
-
-  // row maximum and normaliser (base-2 units) in one pass: each thread merges
-  // its chunks online, then the block merges the (max, sum) pairs
-  float m = -INFINITY, zs = 0.f;
-  for (int c = tid; c < p.n_chunks; c += kSampleThreads) {
-    const float2 e = crow[c];
-    if (e.x > -INFINITY) {
-      if (e.x > m) {
-        zs = (m > -INFINITY ? zs * exp2f(m - e.x) : 0.f) + e.y;
-        m = e.x;
-      } else {
-        zs += e.y * exp2f(e.x - m);
+// Waits until *word >= target (acquire).  Gives up after kWaitLimitNs or once
+// any CTA has raised the abort word; then raises it too and returns false.
+// One thread per waiting group polls, with a short sleep between polls, so
+// that waiters do not crowd L2 while other CTAs still stream.
+__device__ __forceinline__ bool wait_at_least(const uint32_t* word, uint32_t target, uint32_t* abort_word) {
+  if (ld_acquire_gpu(word) >= target) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(word) >= target) return true;
+    if ((i & 15u) == 0u) {
+      if (ld_relaxed_gpu(abort_word)) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        atomicExch(abort_word, 1u);
+        return false;
       }
     }
   }
-  const float M = block_max_f(m, s_redf);
-  const float Z = block_sum_f(m > -INFINITY ? zs * exp2f(m - M) : 0.f, s_redz);
-  auto chunk_w = [&](int c) -> float {
-    const float2 e = crow[c];
-    return e.x > -INFINITY ? e.y * exp2f(e.x - M) : 0.f;
-  };
-  if (!(fabsf(M) <= 3.4e38f) || !(Z > 0.f) || !(Z <= 3.4e38f)) {
-    if (tid == 0) {
-      report(p.status, DSPARK_STATUS_NONFINITE);
-      p.tokens[out] = 0;
-      p.pd_tok[out] = 0.f;
-      p.logZ[out] = NAN;
-    }
-    return;
-  }
-  const float u = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(p.step), kDraftSample);
-  const float target = u * Z;
-  float before_c = 0.f;
-  const int cstar = block_find_crossing<kSampleThreads>(p.n_chunks, 0.f, target, chunk_w, &before_c, sc);
-  const int tb = static_cast<int>((static_cast<long long>(cstar) * p.n_tiles) / p.n_chunks);
-  const int te = static_cast<int>((static_cast<long long>(cstar + 1) * p.n_tiles) / p.n_chunks);
-  const float2* frow = p.fine + r;
-  auto sub_w = [&](int i) -> float {
-    const float2 e = frow[static_cast<size_t>(2 * tb + i) * p.R_pad];
-    return e.x > -INFINITY ? e.y * exp2f(e.x - M) : 0.f;
-  };
-  float before_s = 0.f;
-  const int sstar = 2 * tb + block_find_crossing<kSampleThreads>(2 * (te - tb), before_c, target, sub_w, &before_s, sc);
+}
 
-  // recompute the 32 logits of that sub-tile: column = lane, rank split over
-  // the warps; every W2 load of a thread is issued before the first FMA
-  const int v = sstar * kSubN + lane;
-  const int per = p.rank / (kSampleThreads / 32);  // <= 32
-  float acc = 0.f;
-  if (v < p.V) {
-    const uint16_t* col = p.W2 + static_cast<size_t>(wid * per) * p.V + v;
-    uint16_t wv[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) wv[i] = i < per ? col[static_cast<size_t>(i) * p.V] : 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < per) acc = fmaf(s_e[wid * per + i], __uint_as_float(static_cast<uint32_t>(wv[i]) << 16), acc);
-  }
-  s_part[wid][lane] = acc;
-  __syncthreads();
-  if (wid == 0) {
-    float y = -INFINITY, w = 0.f;
-    if (v < p.V) {
-      float b = 0.f;
-#pragma unroll
-      for (int k = 0; k < kSampleThreads / 32; ++k) b += s_part[k][lane];
-      y = (b + p.U[(static_cast<size_t>(r) * p.gamma + p.step) * p.V + v]) * p.scale;
-      w = exp2f(y - M);
-    }
-    const float incl = before_s + warp_incl_scan_f(w);
-    const unsigned cross = __ballot_sync(0xffffffffu, incl > target && w > 0.f);
-    int pick;
+// First item of a contiguous list of weights w[0..n) (shared memory) whose
+// running sum (from `base`) exceeds `target`, 32 items per round across the
+// warp.  Rounding can leave the total at or below the target: then the last
+// item with positive weight.  `before` = the running sum just before the
+// returned item.  Rolled: it runs once per request and position, so its code
+// size matters more than its loop overhead.
+struct Crossing {
+  int idx;
+  float before;
+};
+__device__ __forceinline__ Crossing warp_crossing(const float* w, int n, float base, float target) {
+  const int lane = threadIdx.x & 31;
+  float run = base;
+  Crossing last = {-1, base};
+  for (int k0 = 0; k0 < n; k0 += 32) {
+    const float wk = k0 + lane < n ? w[k0 + lane] : 0.f;
+    const float incl = warp_incl_scan_f(wk);
+    const float excl = incl - wk;
+    const unsigned cross = __ballot_sync(0xffffffffu, run + incl > target && wk > 0.f);
     if (cross) {
-      pick = __ffs(cross) - 1;
-    } else {
-      const unsigned nz = __ballot_sync(0xffffffffu, w > 0.f);
-      pick = nz ? 31 - __clz(nz) : 0;
+      const int l = __ffs(cross) - 1;
+      return Crossing{k0 + l, run + __shfl_sync(0xffffffffu, excl, l)};
     }
-    const float ypick = __shfl_sync(0xffffffffu, y, pick);
+    const unsigned nz = __ballot_sync(0xffffffffu, wk > 0.f);
+    if (nz) {
+      const int l = 31 - __clz(nz);
+      last = Crossing{k0 + l, run + __shfl_sync(0xffffffffu, excl, l)};
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (last.idx < 0) last.idx = 0;
+  return last;
+}
+
+// First 64-column tile of chunk c when n_tiles tiles are split into n_chunks
+// contiguous chunks.  32-bit: c <= kMaxSampleChunks and n_tiles < 2^18 (the
+// host limits V to 2^24), so c * n_tiles < 2^26.
+__device__ __forceinline__ int chunk_first_tile(int c, int n_tiles, int n_chunks) {
+  return static_cast<int>(static_cast<uint32_t>(c) * static_cast<uint32_t>(n_tiles) / static_cast<uint32_t>(n_chunks));
+}
+
+// Tree reductions over 32 registers (depth 5 instead of a 31-long chain).
+__device__ __forceinline__ float tree_max32(const float (&z)[32]) {
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = fmaxf(z[i], z[i + 16]);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+  return t[0];
+}
+__device__ __forceinline__ float tree_sum32(const float (&z)[32]) {
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = z[i] + z[i + 16];
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] += t[i + w];
+  return t[0];
+}
+// Maximum and the lowest column index attaining it (z[k] is column k).
+__device__ __forceinline__ float tree_argmax32(const float (&z)[32], int* idx) {
+  float t[16];
+  int ix[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    // pairs (i, i + 16): the right one wins only when strictly larger
+    const bool r = z[i + 16] > z[i];
+    t[i] = r ? z[i + 16] : z[i];
+    ix[i] = r ? i + 16 : i;
+  }
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const bool r = t[i + w] > t[i] || (t[i + w] == t[i] && ix[i + w] < ix[i]);
+      t[i] = r ? t[i + w] : t[i];
+      ix[i] = r ? ix[i + w] : ix[i];
+    }
+  *idx = ix[0];
+  return t[0];
+}
+
+// Counts request r's token as published on its M-tile after bringing the next
+// position's W1 row into L2 (one warp; lane 0 counts).
+__device__ __forceinline__ void publish_token(const DraftArgs& p, int r, int step, int x) {
+  if (step + 1 >= p.gamma) return;
+  const int lane = threadIdx.x & 31;
+  if (lane * 128 < p.rank * 2)
+    prefetch_l2(reinterpret_cast<const uint8_t*>(p.W1 + static_cast<size_t>(x) * p.rank) + lane * 128);
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    atomicAdd(p.ready + 16 * (r / kMTile), 1u);
+  }
+}
+
+// Greedy sampler for request r (one warp, every chunk partial of its M-tile
+// visible): the argmax of the chunk partials, lowest index on ties.
+__device__ __forceinline__ void sample_greedy(const DraftArgs& p, int r, int step) {
+  const int lane = threadIdx.x & 31;
+  const size_t out = static_cast<size_t>(r) * p.gamma + step;
+  const float2* crow = p.coarse + static_cast<size_t>(r) * p.n_chunks;
+  float best = -INFINITY;
+  int bidx = 0x7fffffff;
+#pragma unroll
+  for (int k = 0; k < kMaxSampleChunks / 32; ++k) {
+    const int c = k * 32 + lane;
+    const float2 e = c < p.n_chunks ? crow[c] : make_float2(-INFINITY, 0.f);
+    const int ei = __float_as_int(e.y);
+    if (e.x > best || (e.x == best && e.x > -INFINITY && ei < bidx)) { best = e.x; bidx = ei; }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+    if (ob > best || (ob == best && oi < bidx)) { best = ob; bidx = oi; }
+  }
+  if (!(fabsf(best) <= 3.4e38f) || bidx < 0 || bidx >= p.V) {
+    if (lane == 0) report(p.status, DSPARK_STATUS_NONFINITE);
+    bidx = 0;
+  }
+  if (lane == 0) {
+    p.tokens[out] = bidx;
+    p.pd_tok[out] = 1.0f;
+    p.logZ[out] = best;
+  }
+  publish_token(p, r, step, bidx);
+}
+
+// What the leader warp hands to the other sampling warps of its CTA.
+struct SampleSlot {
+  int state;  // 0: gave up waiting (abort), 1: non-finite row, 2: sample
+  int sstar;  // 32-column sub-tile holding the crossing
+  float M, Z, target, before_s;
+  int pad[2];
+};
+constexpr int kSlotSample = 2, kSlotNonFinite = 1, kSlotAbort = 0;
+
+// Shared-memory pieces of the sampler (one per CTA).
+struct SampleSmem {
+  SampleSlot* slot;
+  float* part;      // [8 warps][32 columns] shares of the bias
+  float* wts;       // [kMaxSampleChunks] search weights of the leader
+  uint8_t* slab;    // [rank][32] bf16: W2 columns of the chosen sub-tile, then U of the sub-tile (32 fp32)
+  uint32_t slab_s;  // shared-space address of `slab`
+  uint32_t bar;     // mbarrier of the slab copies
+};
+
+// Inverse-CDF sampler for request r, run by all 8 epilogue warps of the CTA
+// (`sub` = warp index 0..7, named barrier 5).  `phase` counts the slab copies
+// this CTA has waited for.  The leader warp (sub 0) waits until every chunk
+// partial of the M-tile is visible, merges the chunk partials into the row's
+// max M and normaliser Z (base 2), finds the chunk, then the 32-column
+// sub-tile, where the running mass first exceeds u * Z (search weights in
+// shared memory), and copies that sub-tile's W2 columns (one TMA box,
+// rank x 32) and U values (one bulk copy) into shared memory.  Each warp then
+// sums its 32 rank rows for the 32 columns (a lane per column), and the leader
+// adds the shares and U and picks the token.  Returns false (the same in every
+// warp: it follows the slot, read after a barrier) when the leader's wait gave
+// up.
+__device__ __forceinline__ bool sample_cta(const DraftArgs& p, const CUtensorMap* tm_slab, int r, int step, int sub,
+                                        const SampleSmem& sm, uint32_t& phase, volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  const size_t out = static_cast<size_t>(r) * p.gamma + step;
+  SampleSlot& slot = *sm.slot;
+
+  // issued before the wait: the previous token's W1 entry of this lane's rank row
+  const int prev_raw = step == 0 ? p.anchors[r] : p.tokens[out - 1];
+  const int prev = (prev_raw >= 0 && prev_raw < p.V) ? prev_raw : 0;
+  const int j = sub * 32 + lane;  // rank rows j, j + 256 (rank <= 256: one row)
+  const float ev = j < p.rank ? bf16_at(p.W1 + static_cast<size_t>(prev) * p.rank + j) : 0.f;
+
+  if (sub == 0) {
+    const float u = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(step), kDraftSample);
+    bool ok = true;
+    if (lane == 0)
+      ok = wait_at_least(p.done + 16 * (r / kMTile), static_cast<uint32_t>(p.n_chunks * (step + 1)), p.abort);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    int state = kSlotAbort, sstar = 0;
+    float M = 0.f, Z = 0.f, target = 0.f, before_s = 0.f;
+    if (ok) {
+      constexpr int KC = kMaxSampleChunks / 32;
+      const float2* crow = p.coarse + static_cast<size_t>(r) * p.n_chunks;
+      float2 e[KC];
+#pragma unroll
+      for (int k = 0; k < KC; ++k) {
+        const int c = k * 32 + lane;
+        e[k] = c < p.n_chunks ? crow[c] : make_float2(-INFINITY, 0.f);
+      }
+      // two passes: the row maximum, then each chunk's mass in units of 2^M
+      // (the chunk search reuses the masses as its weights)
+      float m = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < KC; ++k) m = fmaxf(m, e[k].x);
+      M = warp_max(m);
+      float zs = 0.f;
+#pragma unroll
+      for (int k = 0; k < KC; ++k) {
+        const float wk = e[k].x > -INFINITY ? e[k].y * ex2(e[k].x - M) : 0.f;
+        sm.wts[k * 32 + lane] = wk;
+        zs += wk;
+      }
+      Z = warp_sum(zs);
+      if (!(fabsf(M) <= 3.4e38f) || !(Z > 0.f) || !(Z <= 3.4e38f)) {
+        state = kSlotNonFinite;
+      } else {
+        state = kSlotSample;
+        target = u * Z;
+        __syncwarp();
+        const Crossing cc = warp_crossing(sm.wts, p.n_chunks, 0.f, target);
+        const int tb = chunk_first_tile(cc.idx, p.n_tiles, p.n_chunks);
+        const int te = chunk_first_tile(cc.idx + 1, p.n_tiles, p.n_chunks);
+        const int nsub = 2 * (te - tb);  // <= kMaxSampleChunks (host check)
+        float2 f[KC];
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+          const int i = k * 32 + lane;
+          f[k] = i < nsub ? p.fine[static_cast<size_t>(2 * tb + i) * p.R_pad + r] : make_float2(-INFINITY, 0.f);
+        }
+        __syncwarp();  // every lane is done reading the chunk weights
+#pragma unroll
+        for (int k = 0; k < KC; ++k) sm.wts[k * 32 + lane] = f[k].x > -INFINITY ? f[k].y * ex2(f[k].x - M) : 0.f;
+        __syncwarp();
+        const Crossing cs = warp_crossing(sm.wts, nsub, cc.before, target);
+        sstar = 2 * tb + cs.idx;
+        before_s = cs.before;
+        if (lane == 0) {
+          // the previous request's readers of the slab are past the barrier
+          fence_proxy_async_smem();
+          // W2[:, v0 .. v0+31] (columns past V zero-filled) and U[r, step, v0 .. v0+31]
+          const int v0 = sstar * kSubN;
+          const uint32_t ubytes = static_cast<uint32_t>(min(kSubN, p.V - v0)) * 4u;  // a multiple of 32
+          mbar_arrive_expect_tx(sm.bar, static_cast<uint32_t>(p.rank) * 64u + ubytes);
+          tma_load_2d(sm.slab_s, tm_slab, sm.bar, v0, 0, policy_evict_normal());
+          bulk_load(sm.slab_s + p.rank * 64, p.U + out * p.V + v0, ubytes, sm.bar, policy_evict_first());
+        }
+      }
+    }
     if (lane == 0) {
-      const int x = min(sstar * kSubN + pick, p.V - 1);
-      p.tokens[out] = x;
-      p.pd_tok[out] = exp2f(ypick - M) / Z;
-      p.logZ[out] = (M + log2f(Z)) * 0.69314718f;
+      slot.state = state;
+      slot.sstar = sstar;
+      slot.M = M;
+      slot.Z = Z;
+      slot.target = target;
+      slot.before_s = before_s;
     }
+  }
+  named_barrier(5, kEpiThreads);
+  const int state = *reinterpret_cast<volatile int*>(&slot.state);
+  const int sstar = *reinterpret_cast<volatile int*>(&slot.sstar);
+
+  bool landed = true;
+  if (state == kSlotSample) {
+    landed = __all_sync(0xffffffffu, mbar_wait(sm.bar, phase & 1u, abort_flag));
+    if (!landed) *abort_flag = 1;
+    ++phase;
+    // this warp's share of the 32 bias values: lane l sums column v0 + l over
+    // the warp's rank rows (W1 entries broadcast from the lane that holds them)
+    float acc = 0.f;
+    if (landed) {
+      const uint16_t* slab = reinterpret_cast<const uint16_t*>(sm.slab);
+#pragma unroll 8
+      for (int k = 0; k < 32; ++k) {
+        const int jk = sub * 32 + k;
+        const float ek = __shfl_sync(0xffffffffu, ev, k);
+        if (jk < p.rank) acc = fmaf(ek, __uint_as_float(static_cast<uint32_t>(slab[jk * 32 + lane]) << 16), acc);
+      }
+    }
+    sm.part[sub * 32 + lane] = acc;
+  }
+  named_barrier(5, kEpiThreads);
+  // A copy that never landed has set the abort flag (reported as
+  // DSPARK_STATUS_TIMEOUT); the row is finished with zero shares so that every
+  // warp takes the same path through the barriers.
+
+  if (sub == 0 && state != kSlotAbort) {
+    int x = 0;
+    if (state == kSlotNonFinite) {
+      if (lane == 0) {
+        report(p.status, DSPARK_STATUS_NONFINITE);
+        p.tokens[out] = 0;
+        p.pd_tok[out] = 0.f;
+        p.logZ[out] = NAN;
+      }
+    } else {
+      const float M = slot.M, Z = slot.Z, target = slot.target, before_s = slot.before_s;
+      float bias = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < kEpiThreads / 32; ++s2) bias += sm.part[s2 * 32 + lane];
+      const int v0 = sstar * kSubN;
+      const int v = v0 + lane;
+      float y = -INFINITY, w = 0.f;
+      if (v < p.V) {
+        y = (bias + reinterpret_cast<const float*>(sm.slab + p.rank * 64)[lane]) * p.scale;
+        w = ex2(y - M);
+      }
+      const float incl = before_s + warp_incl_scan_f(w);
+      const unsigned cross = __ballot_sync(0xffffffffu, incl > target && w > 0.f);
+      int pick;
+      if (cross) {
+        pick = __ffs(cross) - 1;
+      } else {
+        const unsigned nz = __ballot_sync(0xffffffffu, w > 0.f);
+        pick = nz ? 31 - __clz(nz) : 0;
+      }
+      const float ypick = __shfl_sync(0xffffffffu, y, pick);
+      x = min(v0 + pick, p.V - 1);
+      if (lane == 0) {
+        p.tokens[out] = x;
+        p.pd_tok[out] = __fdividef(ex2(ypick - M), Z);
+        p.logZ[out] = (M + __log2f(Z)) * 0.69314718f;
+      }
+    }
+    publish_token(p, r, step, x);
+  }
+  // the slot, the shares and the slab are rewritten for the next request only
+  // after that request's first barrier, which the leader reaches only after
+  // it has finished reading them here
+  return state != kSlotAbort;
+}
+
+template <bool kGreedy>
+__global__ void __launch_bounds__(kDraftThreads, 1)
+    k_markov_draft(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u,
+                   const __grid_constant__ CUtensorMap tm_slab, const DraftArgs p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const DraftSmem plan = draft_smem_plan(p.rank);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mtile = blockIdx.x % p.n_mtiles;
+  const int chunk = blockIdx.x / p.n_mtiles;
+  const int r0 = mtile * kMTile;
+  const int rows_valid = min(kMTile, p.R - r0);
+  const int t_begin = chunk_first_tile(chunk, p.n_tiles, p.n_chunks);
+  const int t_end = chunk_first_tile(chunk + 1, p.n_tiles, p.n_chunks);
+  const int ntile = t_end - t_begin;
+  const int total_tiles = ntile * p.gamma;
+
+  const uint32_t bar_wfull = base + plan.bars;               // [kDraftWStages]
+  const uint32_t bar_wempty = bar_wfull + 8 * kDraftWStages;  // [kDraftWStages]
+  const uint32_t bar_ufull = bar_wempty + 8 * kDraftWStages;  // [kDraftUStages]
+  const uint32_t bar_uempty = bar_ufull + 8 * kDraftUStages;  // [kDraftUStages]
+  const uint32_t bar_tfull = bar_uempty + 8 * kDraftUStages;  // [2]
+  const uint32_t bar_tempty = bar_tfull + 16;                 // [2]
+  const uint32_t bar_slab = bar_tempty + 16;                  // the sampler's slab copies
+  constexpr uint32_t kBarBytes = 16 * (kDraftWStages + kDraftUStages) + 40;
+  static_assert(kBarBytes + 8 <= 256, "barrier block");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + plan.bars + kBarBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + plan.bars + kBarBytes + 4);
+  float2* s_half = reinterpret_cast<float2*>(gbase + plan.half);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDraftWStages; ++s) {
+      mbar_init(bar_wfull + 8 * s, 1);
+      mbar_init(bar_wempty + 8 * s, 1);
+    }
+    for (int s = 0; s < kDraftUStages; ++s) {
+      mbar_init(bar_ufull + 8 * s, 1);
+      mbar_init(bar_uempty + 8 * s, 8);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_tfull + 8 * s, 1);
+      mbar_init(bar_tempty + 8 * s, 8);
+    }
+    mbar_init(bar_slab, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tm_w2);
+    prefetch_tensormap(&tm_u);
+    prefetch_tensormap(&tm_slab);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tmem_a = tmem_base + kAccCols;  // A operand columns
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer (all positions, lane 0)
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_last();
+      const uint64_t pol_u = policy_evict_first();
+      const uint32_t wbytes = 128u * p.rank;
+      int wfilled = 0, ufilled = 0;
+      for (int it = 0; it < total_tiles; ++it) {
+        const int step = it / ntile;
+        const int v0 = (t_begin + (it - step * ntile)) * kTileN;
+        const int sw = it % kDraftWStages, su = it % kDraftUStages;
+        if (!mbar_wait(bar_wempty + 8 * sw, ((it / kDraftWStages) & 1) ^ 1, abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(bar_wfull + 8 * sw, wbytes);
+        tma_load_2d(base + plan.w[sw], &tm_w2, bar_wfull + 8 * sw, v0, 0, pol_w);
+        ++wfilled;
+        if (!mbar_wait(bar_uempty + 8 * su, ((it / kDraftUStages) & 1) ^ 1, abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
+        // one 128-row x 68-column box; rows past R and columns past V are zero-filled
+        mbar_arrive_expect_tx(bar_ufull + 8 * su, kDraftUBytes);
+        tma_load_3d(base + plan.u[su], &tm_u, bar_ufull + 8 * su, v0, step, r0, pol_u);
+        ++ufilled;
+      }
+      if (*abort_flag) {
+        // let copies already in flight land before the CTA exits
+        const uint64_t t0 = global_ns();
+        for (int i = max(0, wfilled - kDraftWStages); i < wfilled; ++i)
+          while (!mbar_try_wait(bar_wfull + 8 * (i % kDraftWStages), (i / kDraftWStages) & 1) &&
+                 global_ns() - t0 < kWaitLimitNs) {
+          }
+        for (int i = max(0, ufilled - kDraftUStages); i < ufilled; ++i)
+          while (!mbar_try_wait(bar_ufull + 8 * (i % kDraftUStages), (i / kDraftUStages) & 1) &&
+                 global_ns() - t0 < kWaitLimitNs) {
+          }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- UMMA issuer
+    const uint32_t idesc = idesc_bf16_f32(kMTile, kTileN, false, true);
+    const int ksteps = p.rank / 16;
+    int issued = 0;
+    for (int step = 0; step < p.gamma; ++step) {
+      named_barrier(2, kEpiThreads + 32);  // this position's A operand is in tensor memory
+      tc_fence_after_sync();
+      if (lane == 0 && !*abort_flag) {
+        for (int i = 0; i < ntile; ++i) {
+          const int it = step * ntile + i;
+          const int sw = it % kDraftWStages, acc = it & 1;
+          if (!mbar_wait(bar_wfull + 8 * sw, (it / kDraftWStages) & 1, abort_flag) ||
+              !mbar_wait(bar_tempty + 8 * acc, ((it >> 1) & 1) ^ 1, abort_flag)) {
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
+          for (int ks = 0; ks < ksteps; ++ks) {
+            const uint32_t b_addr = base + plan.w[sw] + ks * 2048;
+            umma_bf16_ts(d, tmem_a + ks * 8, smem_desc_sw128(b_addr, 1024, 1024), idesc, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(bar_wempty + 8 * sw);
+          umma_commit(bar_tfull + 8 * acc);
+          issued = it + 1;
+        }
+      }
+      __syncwarp();
+    }
+    if (lane == 0 && *abort_flag && issued > 0) {
+      const int i = issued - 1;
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(bar_tfull + 8 * (i & 1), (i >> 1) & 1) && global_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue + sampler warps 2..9
+    const int q = warp & 3;         // tensor-memory lane quarter of this warp
+    const int h = (warp - 2) >> 2;  // 32-column half of each tile; half of A's columns
+    const int row = q * 32 + lane;
+    const int r = r0 + row;
+    const bool valid = row < rows_valid;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const int half_u4 = p.rank / 16;  // uint4 (8 bf16) per half of a W1 row
+    SampleSmem ssm;
+    ssm.slot = reinterpret_cast<SampleSlot*>(gbase + plan.slots);
+    ssm.part = reinterpret_cast<float*>(gbase + plan.part);
+    ssm.wts = reinterpret_cast<float*>(gbase + plan.wts);
+    ssm.slab = gbase + plan.slab;
+    ssm.slab_s = base + plan.slab;
+    ssm.bar = bar_slab;
+    uint32_t slab_phase = 0;  // slab copies this CTA has waited for
+
+    for (int step = 0; step < p.gamma; ++step) {
+      // ---- gather: W1[x_{step-1}] of this row, K elements [h*rank/2, (h+1)*rank/2),
+      // once every token of this M-tile's previous position is published (one
+      // poller per CTA).  Every abort decision is warp-uniform: tensor-memory
+      // loads and stores are warp-collective.
+      if (step > 0) {
+        if (threadIdx.x == 64 && !*abort_flag &&
+            !wait_at_least(p.ready + 16 * mtile, static_cast<uint32_t>(rows_valid * step), p.abort))
+          *abort_flag = 1;
+        named_barrier(4, kEpiThreads);
+      }
+      if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
+        int tok = -1;
+        if (valid) {
+          tok = step == 0 ? p.anchors[r] : p.tokens[static_cast<size_t>(r) * p.gamma + step - 1];
+          if (tok < 0 || tok >= p.V) {
+            report(p.status, DSPARK_STATUS_BAD_TOKEN);
+            tok = 0;
+          }
+        }
+        const uint4* src =
+            reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(tok < 0 ? 0 : tok) * p.rank) + h * half_u4;
+        uint32_t a[64];  // all loads first, then the tensor-memory stores
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          uint4 wv = make_uint4(0, 0, 0, 0);
+          if (tok >= 0 && k < half_u4) wv = __ldg(src + k);
+          a[4 * k] = wv.x; a[4 * k + 1] = wv.y; a[4 * k + 2] = wv.z; a[4 * k + 3] = wv.w;
+        }
+        const uint32_t dst = tmem_a + lane_off + static_cast<uint32_t>(h * 4 * half_u4);
+        const uint32_t(&a0)[32] = *reinterpret_cast<const uint32_t(*)[32]>(&a[0]);
+        const uint32_t(&a1)[32] = *reinterpret_cast<const uint32_t(*)[32]>(&a[32]);
+        if (half_u4 >= 8) {
+          tmem_st_32x32(dst, a0);
+          if (half_u4 == 16) tmem_st_32x32(dst + 32, a1);
+          else if (half_u4 == 12) tmem_st_32x16(dst + 32, a1);
+        } else {
+          tmem_st_32x16(dst, a0);  // rank 64
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before_sync();
+      named_barrier(2, kEpiThreads + 32);
+
+      // ---- tiles
+      float runM = -INFINITY, runS = 0.f;  // running (max, sum exp2) of this warp's half of the chunk
+      int runIdx = 0;                      // greedy: running argmax
+      if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
+        for (int i = 0; i < ntile; ++i) {
+          const int it = step * ntile + i;
+          const int su = it % kDraftUStages, acc = it & 1;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, (it >> 1) & 1, abort_flag))) {
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after_sync();
+          float z[32];
+          tmem_ld_32x32(tmem_base + lane_off + static_cast<uint32_t>(acc * kTileN + h * kSubN), z);
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_ufull + 8 * su, (it / kDraftUStages) & 1, abort_flag))) {
+            *abort_flag = 1;
+            break;
+          }
+          const float4* urow =
+              reinterpret_cast<const float4*>(gbase + plan.u[su] + row * (kDraftUCols * 4) + h * (kSubN * 4));
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float4 t4 = urow[k];
+            z[4 * k] += t4.x; z[4 * k + 1] += t4.y; z[4 * k + 2] += t4.z; z[4 * k + 3] += t4.w;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_uempty + 8 * su);
+
+          // z = bias + U of 32 columns; columns past V only in the last tile
+          const int v0 = (t_begin + i) * kTileN + h * kSubN;
+          const int ncol = min(kSubN, p.V - v0);
+          if (ncol < kSubN) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) z[k] = k < ncol ? z[k] : -INFINITY;
+          }
+          const size_t fidx = static_cast<size_t>(2 * (t_begin + i) + h) * p.R_pad + r;
+          if constexpr (kGreedy) {
+            int k;
+            const float mx = tree_argmax32(z, &k);
+            const int ix = v0 + k;
+            if (valid) p.fine[fidx] = make_float2(mx, __int_as_float(ix));
+            if (mx > runM) { runM = mx; runIdx = ix; }
+          } else {
+            // y = z * log2(e)/T; partial (max y, sum exp2(y - max y))
+            const float mz = tree_max32(z);
+            float mx = -INFINITY, sm = 0.f;
+            if (mz > -INFINITY) {
+              mx = mz * p.scale;
+#pragma unroll
+              for (int k = 0; k < 32; ++k) z[k] = ex2(fmaf(z[k], p.scale, -mx));
+              sm = tree_sum32(z);
+            }
+            if (valid) p.fine[fidx] = make_float2(mx, sm);
+            if (mx > -INFINITY) {
+              if (mx > runM) {
+                runS = (runM > -INFINITY ? runS * ex2(runM - mx) : 0.f) + sm;
+                runM = mx;
+              } else {
+                runS += sm * ex2(mx - runM);
+              }
+            }
+          }
+        }
+      }
+      // ---- combine the two column halves of this CTA's chunk
+      if (h == 1) s_half[row] = kGreedy ? make_float2(runM, __int_as_float(runIdx)) : make_float2(runM, runS);
+      named_barrier(1, kEpiThreads);
+      if (h == 0 && valid && !*abort_flag) {
+        const float2 o = s_half[row];
+        float2 outv;
+        if constexpr (kGreedy) {
+          const int oi = __float_as_int(o.y);
+          if (o.x > runM || (o.x == runM && oi < runIdx)) { runM = o.x; runIdx = oi; }
+          outv = make_float2(runM, __int_as_float(runIdx));
+        } else {
+          const float Mx = fmaxf(runM, o.x);
+          float S = 0.f;
+          if (Mx > -INFINITY) {
+            if (runM > -INFINITY) S += runS * ex2(runM - Mx);
+            if (o.x > -INFINITY) S += o.y * ex2(o.x - Mx);
+          }
+          outv = make_float2(Mx, S);
+        }
+        p.coarse[static_cast<size_t>(r) * p.n_chunks + chunk] = outv;
+      }
+      // ---- this CTA is done with the position: count it on its M-tile
+      named_barrier(3, kEpiThreads);
+      if (threadIdx.x == 64 && !*abort_flag) {
+        __threadfence();
+        atomicAdd(p.done + 16 * mtile, 1u);
+      }
+
+      // ---- sample this CTA's requests once every chunk of their M-tile is done
+      if constexpr (kGreedy) {
+        // one warp per request
+        for (int rr = blockIdx.x + gridDim.x * (warp - 2); rr < p.R; rr += gridDim.x * (kEpiThreads / 32)) {
+          bool ok = true;
+          if (lane == 0)
+            ok = !*abort_flag && wait_at_least(p.done + 16 * (rr / kMTile),
+                                               static_cast<uint32_t>(p.n_chunks * (step + 1)), p.abort);
+          if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            *abort_flag = 1;
+            break;
+          }
+          sample_greedy(p, rr, step);
+        }
+      } else {
+        // all 8 epilogue warps on each of this CTA's requests in turn
+        for (int rr = blockIdx.x; rr < p.R; rr += gridDim.x) {
+          if (!sample_cta(p, &tm_slab, rr, step, warp - 2, ssm, slab_phase, abort_flag)) {
+            *abort_flag = 1;
+            break;
+          }
+        }
+      }
+    }
+  }
+  if (*abort_flag && threadIdx.x == 0) report(p.status, DSPARK_STATUS_TIMEOUT);
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -220,17 +817,32 @@ int encode_w2_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank) {
   return rc == CUDA_SUCCESS ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
+// W2 [rank, V] bf16 again, box 32 x rank without swizzle: the sampler's copy
+// of the 32 columns of one sub-tile ([rank][32], 64-byte rows).
+int encode_w2_slab_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank) {
+  auto fn = get_encode_fn();
+  if (!fn) return DSPARK_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(rank)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kSubN), static_cast<cuuint32_t>(rank)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult rc = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W2), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
 // U [R, gamma, V] fp32 as a 3-D tensor (x = vocabulary, y = position,
-// z = request); box 32 x 1 x 128 with 128-byte swizzle.
+// z = request); box 68 x 1 x 128, no swizzle (see kDraftUCols).
 int encode_u_map(CUtensorMap* tm, const float* U, int R, int gamma, int V) {
   auto fn = get_encode_fn();
   if (!fn) return DSPARK_ERR_CUDA;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(gamma), static_cast<cuuint64_t>(R)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(V) * 4, static_cast<cuuint64_t>(V) * 4 * gamma};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kSubN), 1, static_cast<cuuint32_t>(kMTile)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kDraftUCols), 1, static_cast<cuuint32_t>(kMTile)};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult rc = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(U), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return rc == CUDA_SUCCESS ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
@@ -243,69 +855,58 @@ int vocab_chunks(int n_tiles, int n_mtiles) {
   return c;
 }
 
-// pdl: whether this launch may overlap the tail of the previous kernel in the
-// stream.  A draft pass reads U and W2 before its griddepcontrol.wait, so the
-// first pass of a call is launched without it: whatever precedes the call on
-// the stream (for instance the kernel that produced U) completes first.
-cudaError_t launch_vocab_partials(VocabMode mode, const CUtensorMap& tm_w2, const CUtensorMap& tm_u,
-                                  const VocabArgs& a, cudaStream_t stream, bool pdl) {
-  const VocabSmem plan = vocab_smem_plan(a.rank);
-  const dim3 grid(a.n_chunks * a.n_mtiles);
-  const int max_smem = static_cast<int>(vocab_smem_plan(256).total);
-  if (mode == VocabMode::kDraft) {
-    static std::once_flag once;
-    std::call_once(once, [&] {
-      cudaFuncSetAttribute(k_vocab_partials<VocabMode::kDraft>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    });
-    return launch_pdl(k_vocab_partials<VocabMode::kDraft>, grid, dim3(kDraftThreads), plan.total, stream, pdl, tm_w2,
-                      tm_u, a);
-  }
-  static std::once_flag once_r;
-  std::call_once(once_r, [&] {
-    cudaFuncSetAttribute(k_vocab_partials<VocabMode::kResidual>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  });
-  return launch_pdl(k_vocab_partials<VocabMode::kResidual>, grid, dim3(kDraftThreads), plan.total, stream, pdl, tm_w2,
-                    tm_u, a);
-}
-
 int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors, int R,
                         int gamma, int V, int rank, float temperature, uint64_t seed, uint32_t round,
                         int32_t* tokens, float* pd_tok, float* logZ, void* workspace, cudaStream_t stream) {
   const WorkspaceLayout L = workspace_layout(R, gamma, V);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  VocabArgs a = {};
-  a.U = U; a.W1 = W1; a.W2 = W2; a.anchors = anchors; a.tokens = tokens;
+  DraftArgs a = {};
+  a.U = U; a.W1 = W1; a.W2 = W2; a.anchors = anchors;
+  a.tokens = tokens; a.pd_tok = pd_tok; a.logZ = logZ;
   a.coarse = reinterpret_cast<float2*>(ws + L.coarse);
   a.fine = reinterpret_cast<float2*>(ws + L.fine);
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
   a.R = R;
   a.n_mtiles = ceil_div(R, kMTile);
+  a.done = reinterpret_cast<uint32_t*>(ws + L.dsync);
+  a.ready = a.done + 16 * a.n_mtiles;
+  a.abort = a.ready + 16 * a.n_mtiles;
   a.R_pad = a.n_mtiles * kMTile;
   a.gamma = gamma; a.V = V; a.rank = rank;
   a.n_tiles = ceil_div(V, kTileN);
   a.n_chunks = vocab_chunks(a.n_tiles, a.n_mtiles);
-  a.greedy = temperature == 0.0f ? 1 : 0;
-  a.scale = a.greedy ? 1.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  const bool greedy = temperature == 0.0f;
+  a.scale = greedy ? 1.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  a.seed = seed; a.round = round;
+  // the sampler holds a row's chunk partials, and the sub-tile partials of
+  // one chunk, in registers
+  if (a.n_chunks > kMaxSampleChunks || 2 * ceil_div(a.n_tiles, a.n_chunks) > kMaxSampleChunks || V > kMaxDraftV)
+    return DSPARK_ERR_UNSUPPORTED_SHAPE;
 
-  SampleArgs s = {};
-  s.U = U; s.W1 = W1; s.W2 = W2; s.anchors = anchors; s.tokens = tokens; s.pd_tok = pd_tok; s.logZ = logZ;
-  s.coarse = a.coarse; s.fine = a.fine; s.status = a.status;
-  s.R = R; s.R_pad = a.R_pad; s.gamma = gamma; s.V = V; s.rank = rank;
-  s.n_tiles = a.n_tiles; s.n_chunks = a.n_chunks; s.scale = a.scale; s.greedy = a.greedy;
-  s.seed = seed; s.round = round;
-
-  CUtensorMap tm_w2, tm_u;
-  if (encode_w2_map(&tm_w2, W2, V, rank) != DSPARK_OK || encode_u_map(&tm_u, U, R, gamma, V) != DSPARK_OK)
+  CUtensorMap tm_w2, tm_u, tm_slab;
+  if (encode_w2_map(&tm_w2, W2, V, rank) != DSPARK_OK || encode_u_map(&tm_u, U, R, gamma, V) != DSPARK_OK ||
+      encode_w2_slab_map(&tm_slab, W2, V, rank) != DSPARK_OK)
     return DSPARK_ERR_CUDA;
-  for (int step = 0; step < gamma; ++step) {
-    a.step = step;
-    s.step = step;
-    if (launch_vocab_partials(VocabMode::kDraft, tm_w2, tm_u, a, stream, step > 0) != cudaSuccess)
-      return DSPARK_ERR_CUDA;
-    if (launch_pdl(k1_sample, dim3(R), dim3(kSampleThreads), 0, stream, true, s) != cudaSuccess)
-      return DSPARK_ERR_CUDA;
-  }
-  return DSPARK_OK;
+
+  const DraftSmem plan = draft_smem_plan(rank);
+  const int max_smem = static_cast<int>(draft_smem_plan(256).total);
+  auto kernel = greedy ? k_markov_draft<true> : k_markov_draft<false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  // done / ready counters and the abort word start at zero on every call
+  if (cudaMemsetAsync(ws + L.dsync, 0, L.dsync_bytes, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_chunks * a.n_mtiles);
+  cfg.blockDim = dim3(kDraftThreads);
+  cfg.dynamicSmemBytes = plan.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident: the grid barriers rely on it
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tm_w2, tm_u, tm_slab, a) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
 }  // namespace dspark

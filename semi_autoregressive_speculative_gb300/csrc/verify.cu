@@ -11,18 +11,20 @@
 //                   accept test u < p_t(x) / p_d(x) position by position, the
 //                   bonus draw from row lens[r] when everything is accepted,
 //                   otherwise the request joins the rejection list.
-//  k_vocab_partials<kResidual>  tensor-core recompute of the draft rows at the
+//  k_residual_partials  tensor-core recompute of the draft rows at the
 //                   rejected positions fused with max(0, p_t - p_d) partial sums.
 //  k4_residual_sample  one CTA per rejected request: inverse CDF of the
 //                   residual (or of p_t when its mass is zero).
 #include <cuda.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "common.h"
 #include "device.cuh"
 #include "search.cuh"
-#include "vocab_gemm.cuh"
+#include "residual.cuh"
+#include "vocab_common.h"
 
 namespace dspark {
 
@@ -384,6 +386,19 @@ __global__ void __launch_bounds__(256) k4_residual_sample(const VerifyArgs p) {
   }
 }
 
+// The residual pass of verify, chained to the accept kernel with programmatic
+// dependent launch.
+static cudaError_t launch_residual_partials(const CUtensorMap& tm_w2, const ResidualArgs& a, cudaStream_t stream) {
+  const ResidualSmem plan = residual_smem_plan(a.rank);
+  const dim3 grid(a.n_chunks * a.n_mtiles);
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(k_residual_partials, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(residual_smem_plan(256).total));
+  });
+  return launch_pdl(k_residual_partials, grid, dim3(kDraftThreads), plan.total, stream, true, tm_w2, a);
+}
+
 int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors,
                   const int32_t* tokens, const float* pd_tok, const float* logZ, const int32_t* lens, int R, int gamma,
                   int V, int rank, float temperature, uint64_t seed, uint32_t round, int32_t* n_accept,
@@ -422,20 +437,18 @@ int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint
     return DSPARK_ERR_CUDA;
   if (p.greedy) return DSPARK_OK;
 
-  VocabArgs a = {};
+  ResidualArgs a = {};
   a.U = U; a.W1 = W1; a.W2 = W2; a.anchors = anchors; a.tokens = tokens;
+  a.T = T; a.rej = p.rej; a.n_acc = n_accept; a.trow = p.trow; a.logZd = logZ;
   a.coarse = reinterpret_cast<float2*>(ws + L.coarse);
   a.fine = reinterpret_cast<float2*>(ws + L.fine);
   a.status = p.status;
-  a.R = R; a.R_pad = p.R_pad; a.gamma = gamma; a.V = V; a.rank = rank; a.step = 0;
+  a.R = R; a.R_pad = p.R_pad; a.gamma = gamma; a.V = V; a.rank = rank;
   a.n_tiles = p.n_tiles; a.n_chunks = p.n_chunks; a.n_mtiles = n_mtiles;
-  a.scale = p.scale; a.greedy = 0;
-  a.T = T; a.rej = p.rej; a.n_acc = n_accept; a.trow = p.trow; a.logZd = logZ;
+  a.scale = p.scale;
   CUtensorMap tm_w2;
   if (encode_w2_map(&tm_w2, W2, V, rank) != DSPARK_OK) return DSPARK_ERR_CUDA;
-  // the residual pass gathers its U rows with bulk copies: no U tensor map
-  if (launch_vocab_partials(VocabMode::kResidual, tm_w2, tm_w2, a, stream, true) != cudaSuccess)
-    return DSPARK_ERR_CUDA;
+  if (launch_residual_partials(tm_w2, a, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   if (launch_pdl(k4_residual_sample, dim3(R), dim3(256), 0, stream, true, p) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   return DSPARK_OK;

@@ -18,6 +18,8 @@ SMALL_CASES = [
     # rank 64 and the smallest vocabulary the boundary accepts
     (synth.scaled(TINY, R=5, gamma=4, V=8, rank=64, d=32, name="v8_rank64"), (1.0, 0.0)),
     (synth.scaled(TINY, R=3, gamma=6, V=4104, rank=192, d=40, name="v4104_rank192"), (0.7, 0.0)),
+    # three M-tiles: samplers of one M-tile run on CTAs of the others
+    (synth.scaled(TINY, R=300, gamma=3, V=2056, d=16, name="r300_three_mtiles"), (1.0, 0.0)),
 ]
 
 
