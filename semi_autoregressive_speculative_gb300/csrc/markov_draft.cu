@@ -74,7 +74,7 @@ struct DraftArgs {
 };
 
 struct DraftSmem {
-  uint32_t w[kDraftWStages], u[kDraftUStages], half, bars, slots, part, wts, slab, total;
+  uint32_t w[kDraftWStages], u[kDraftUStages], half, bars, slots, part, wts, ev, slab, total;
 };
 __host__ __device__ inline DraftSmem draft_smem_plan(int rank) {
   DraftSmem s;
@@ -86,6 +86,7 @@ __host__ __device__ inline DraftSmem draft_smem_plan(int rank) {
   s.slots = off; off += 32;                      // the sampler's SampleSlot
   s.part = off; off += 8 * 32 * 4;               // each epilogue warp's 32 column shares
   s.wts = off; off += kMaxSampleChunks * 4;      // the leader's search weights
+  s.ev = off; off += 256 * 4;                    // the previous token's W1 row
   off = (off + 127u) & ~127u;
   s.slab = off; off += 64u * rank + 32 * 4;      // W2 columns [rank][32] bf16, then 32 U values
   s.total = off + 1024;  // alignment slack
@@ -133,38 +134,52 @@ __device__ __forceinline__ bool wait_at_least(const uint32_t* word, uint32_t tar
   }
 }
 
-// First item of a contiguous list of weights w[0..n) (shared memory) whose
-// running sum (from `base`) exceeds `target`, 32 items per round across the
-// warp.  Rounding can leave the total at or below the target: then the last
-// item with positive weight.  `before` = the running sum just before the
-// returned item.  Rolled: it runs once per request and position, so its code
-// size matters more than its loop overhead.
+// First item of a contiguous list of weights w[0..n) (shared memory, n <= 256)
+// whose running sum (from `base`) exceeds `target`.  Each lane sums its own
+// contiguous segment of ceil(n/32) items, one warp scan over the segment sums
+// finds the lane that crosses, and that lane walks its segment: a single scan
+// however long the list.  Rounding can leave the total at or below the target:
+// then the last item with positive weight.  `before` = the running sum just
+// before the returned item.
 struct Crossing {
   int idx;
   float before;
 };
 __device__ __forceinline__ Crossing warp_crossing(const float* w, int n, float base, float target) {
   const int lane = threadIdx.x & 31;
-  float run = base;
-  Crossing last = {-1, base};
-  for (int k0 = 0; k0 < n; k0 += 32) {
-    const float wk = k0 + lane < n ? w[k0 + lane] : 0.f;
-    const float incl = warp_incl_scan_f(wk);
-    const float excl = incl - wk;
-    const unsigned cross = __ballot_sync(0xffffffffu, run + incl > target && wk > 0.f);
-    if (cross) {
-      const int l = __ffs(cross) - 1;
-      return Crossing{k0 + l, run + __shfl_sync(0xffffffffu, excl, l)};
+  const int seg = (n + 31) >> 5;
+  const int lo = min(n, lane * seg), hi = min(n, lo + seg);
+  float mine = 0.f;
+  for (int i = lo; i < hi; ++i) mine += w[i];
+  const float incl = warp_incl_scan_f(mine);
+  const float start = base + (incl - mine);  // running sum before this lane's segment
+  const unsigned cross = __ballot_sync(0xffffffffu, base + incl > target && mine > 0.f);
+  const unsigned nz = __ballot_sync(0xffffffffu, mine > 0.f);
+  // the owner: the first crossing lane, else the last lane holding mass
+  const int owner = cross ? __ffs(cross) - 1 : (nz ? 31 - __clz(nz) : 0);
+  Crossing c = {lo, start};
+  if (lane == owner) {
+    float run = start;
+    int found = -1, last = -1;
+    float last_before = start;
+    for (int i = lo; i < hi; ++i) {
+      const float wi = w[i];
+      if (wi > 0.f) {
+        if (cross && run + wi > target) { found = i; break; }
+        last = i;
+        last_before = run;
+      }
+      run += wi;
     }
-    const unsigned nz = __ballot_sync(0xffffffffu, wk > 0.f);
-    if (nz) {
-      const int l = 31 - __clz(nz);
-      last = Crossing{k0 + l, run + __shfl_sync(0xffffffffu, excl, l)};
+    if (found >= 0) {
+      c = Crossing{found, run};
+    } else if (last >= 0) {  // no crossing inside the segment (rounding): its last positive item
+      c = Crossing{last, last_before};
     }
-    run += __shfl_sync(0xffffffffu, incl, 31);
   }
-  if (last.idx < 0) last.idx = 0;
-  return last;
+  c.idx = __shfl_sync(0xffffffffu, c.idx, owner);
+  c.before = __shfl_sync(0xffffffffu, c.before, owner);
+  return c;
 }
 
 // First 64-column tile of chunk c when n_tiles tiles are split into n_chunks
@@ -279,6 +294,7 @@ struct SampleSmem {
   SampleSlot* slot;
   float* part;      // [8 warps][32 columns] shares of the bias
   float* wts;       // [kMaxSampleChunks] search weights of the leader
+  float* ev;        // [256] the previous token's W1 row (fp32)
   uint8_t* slab;    // [rank][32] bf16: W2 columns of the chosen sub-tile, then U of the sub-tile (32 fp32)
   uint32_t slab_s;  // shared-space address of `slab`
   uint32_t bar;     // mbarrier of the slab copies
@@ -305,8 +321,8 @@ __device__ __forceinline__ bool sample_cta(const DraftArgs& p, const CUtensorMap
   // issued before the wait: the previous token's W1 entry of this lane's rank row
   const int prev_raw = step == 0 ? p.anchors[r] : p.tokens[out - 1];
   const int prev = (prev_raw >= 0 && prev_raw < p.V) ? prev_raw : 0;
-  const int j = sub * 32 + lane;  // rank rows j, j + 256 (rank <= 256: one row)
-  const float ev = j < p.rank ? bf16_at(p.W1 + static_cast<size_t>(prev) * p.rank + j) : 0.f;
+  const int j = sub * 32 + lane;  // this lane's rank row (rank <= 256: one row per lane)
+  sm.ev[j] = j < p.rank ? bf16_at(p.W1 + static_cast<size_t>(prev) * p.rank + j) : 0.f;
 
   if (sub == 0) {
     const float u = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(step), kDraftSample);
@@ -393,15 +409,14 @@ __device__ __forceinline__ bool sample_cta(const DraftArgs& p, const CUtensorMap
     if (!landed) *abort_flag = 1;
     ++phase;
     // this warp's share of the 32 bias values: lane l sums column v0 + l over
-    // the warp's rank rows (W1 entries broadcast from the lane that holds them)
+    // the warp's rank rows (W1 entries read as shared-memory broadcasts)
     float acc = 0.f;
     if (landed) {
       const uint16_t* slab = reinterpret_cast<const uint16_t*>(sm.slab);
 #pragma unroll 8
       for (int k = 0; k < 32; ++k) {
         const int jk = sub * 32 + k;
-        const float ek = __shfl_sync(0xffffffffu, ev, k);
-        if (jk < p.rank) acc = fmaf(ek, __uint_as_float(static_cast<uint32_t>(slab[jk * 32 + lane]) << 16), acc);
+        if (jk < p.rank) acc = fmaf(sm.ev[jk], __uint_as_float(static_cast<uint32_t>(slab[jk * 32 + lane]) << 16), acc);
       }
     }
     sm.part[sub * 32 + lane] = acc;
@@ -610,6 +625,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
     ssm.slot = reinterpret_cast<SampleSlot*>(gbase + plan.slots);
     ssm.part = reinterpret_cast<float*>(gbase + plan.part);
     ssm.wts = reinterpret_cast<float*>(gbase + plan.wts);
+    ssm.ev = reinterpret_cast<float*>(gbase + plan.ev);
     ssm.slab = gbase + plan.slab;
     ssm.slab_s = base + plan.slab;
     ssm.bar = bar_slab;
