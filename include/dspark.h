@@ -46,7 +46,8 @@ extern "C" {
 
 #define DSPARK_OK 0
 #define DSPARK_ERR_INVALID_ARG (-1)       /* null pointer, negative size, bad temperature, short workspace, misalignment */
-#define DSPARK_ERR_UNSUPPORTED_SHAPE (-2) /* V % 8 != 0, rank not in {64,128,192,256}, gamma > 64, R*gamma > 8192 (schedule) */
+#define DSPARK_ERR_UNSUPPORTED_SHAPE (-2) /* V % 8 != 0, rank not in {64,128,192,256}, gamma > 64,
+                                            R*gamma > 8192 (schedule), V > 2^24 (draft), R > 32768 (verify) */
 #define DSPARK_ERR_CUDA (-3)              /* a kernel launch or CUDA runtime call failed */
 #define DSPARK_ERR_STATIC_SCRATCH_TOO_SMALL (-4) /* dspark_markov_draft_noalloc: shape needs more than
                                                     DSPARK_NOALLOC_SCRATCH_BYTES of scratch */
@@ -84,9 +85,13 @@ int dspark_clear_status(void *workspace, void *stream);
  *   tokens   int32 [R, gamma]     out: drafted tokens
  *   pd_tok   fp32 [R, gamma]      out: p_d(x_j)
  *   logZ     fp32 [R, gamma]      out: log Z_j (natural log, of z_j = logits / T)
- * Sizes: R >= 0, 1 <= gamma <= 64, V >= 8 with V % 8 == 0, rank in {64,128,192,256}.
- * R == 0 enqueues nothing.  Enqueues 2 * gamma kernels (a fused tensor-core
- * bias + softmax-partials kernel and a sampling kernel per position).
+ * Sizes: R >= 0, 1 <= gamma <= 64, 8 <= V <= 2^24 with V % 8 == 0, rank in {64,128,192,256}.
+ * R == 0 enqueues nothing.  Enqueues one zeroing of the workspace's
+ * synchronisation words and one cooperative kernel that keeps every CTA
+ * resident for all gamma positions (one CTA per SM; it fails to launch, with
+ * DSPARK_ERR_CUDA, when R needs more than one M-tile of 128 rows per SM).
+ * The kernel's cross-CTA waits are bounded: a wait that gives up sets
+ * DSPARK_STATUS_TIMEOUT and the outputs are then not valid.
  */
 int dspark_markov_draft(const float *U, const uint16_t *W1, const uint16_t *W2,
                         const int32_t *anchors, int R, int gamma, int V, int rank,
@@ -151,6 +156,7 @@ int dspark_schedule(const float *a, int R, int gamma, const double *sps, int sps
  *   n_accept int32 [R]            out: accepted drafts
  *   next_token int32 [R]          out: correction or bonus token
  * Only rows 0..lens[r] of each request are read.
+ * Sizes: as dspark_markov_draft, and R <= 32768.
  */
 int dspark_verify(const float *T, const float *U, const uint16_t *W1, const uint16_t *W2,
                   const int32_t *anchors, const int32_t *tokens, const float *pd_tok,

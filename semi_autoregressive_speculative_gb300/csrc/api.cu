@@ -100,7 +100,7 @@ int dspark_verify(const float* T, const float* U, const uint16_t* W1, const uint
                   int V, int rank, float temperature, uint64_t seed, uint32_t round, int32_t* n_accept,
                   int32_t* next_token, void* workspace, size_t workspace_bytes, void* stream) {
   if (R < 0 || gamma < 1 || V < 8 || rank < 1 || !finite_nonneg(temperature)) return DSPARK_ERR_INVALID_ARG;
-  if (gamma > kMaxGamma || V % 8 != 0 || !rank_ok(rank)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (gamma > kMaxGamma || V % 8 != 0 || !rank_ok(rank) || R > kMaxVerifyR) return DSPARK_ERR_UNSUPPORTED_SHAPE;
   if (R == 0) return DSPARK_OK;
   if (!T || !U || !W1 || !W2 || !anchors || !tokens || !pd_tok || !logZ || !lens || !n_accept || !next_token ||
       !workspace)

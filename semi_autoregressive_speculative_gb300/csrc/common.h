@@ -22,6 +22,7 @@ constexpr int kDraftThreads = 320; // warp 0 TMA producer, warp 1 MMA, warps 2..
 constexpr int kVerifyChunk = 1024; // target columns per verify statistics item
 constexpr int kMaxGamma = 64;
 constexpr int kMaxSchedule = 8192; // R * gamma handled by the one-CTA scheduler
+constexpr int kMaxVerifyR = 32768; // verify keeps R + 1 row offsets in shared memory
 
 constexpr int kMaxSampleChunks = 256; // chunk partials per row the draft sampler holds in registers
 

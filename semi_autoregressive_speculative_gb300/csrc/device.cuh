@@ -131,34 +131,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
-// Non-blocking test of the phase with the given parity.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-// Polling wait for threads that wait long while other warps work (the TMA
-// producer, the MMA issuer): non-blocking tests with a short sleep between
-// them.  Same give-up rules as mbar_wait.
-__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity, volatile int* abort) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    __nanosleep(32);
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((i & 63u) == 0u) {
-      if (*abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-  }
-}
-
 // Waits for the phase with the given parity to complete.  Gives up (returns
 // false) after kWaitLimitNs or once *abort is set by another warp.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {

@@ -4,7 +4,8 @@
 //
 //  k4_prepare       one CTA: verify-row offsets (exclusive scan of lens + 1),
 //                   clears the rejection list.
-//  k4_target_stats  one warp per (verify row, 1024-column chunk): softmax
+//  k4_target_stats  one warp per (verify row, 1024-column chunk; row owners from a
+//                   shared-memory copy of the row offsets): softmax
 //                   partials of T / temperature (or max / argmax), and the
 //                   target logit at the drafted token.
 //  k4_accept        one CTA per request: per row max and normaliser, the
@@ -99,23 +100,26 @@ __global__ void __launch_bounds__(1024) k4_prepare(const VerifyArgs p) {
 }
 
 __global__ void __launch_bounds__(256) k4_target_stats(const VerifyArgs p) {
+  extern __shared__ int32_t s_rowoff[];  // [R + 1]
   pdl_launch_dependents();
   pdl_wait();
+  for (int i = threadIdx.x; i <= p.R; i += blockDim.x) s_rowoff[i] = p.rowoff[i];
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int nw = gridDim.x * 8;
-  const int rows = p.rowoff[p.R];
+  const int rows = s_rowoff[p.R];
   const long long items = static_cast<long long>(rows) * p.n_vc;
   for (long long it = gw; it < items; it += nw) {
     const int gi = static_cast<int>(it / p.n_vc);
     const int c = static_cast<int>(it - static_cast<long long>(gi) * p.n_vc);
-    // request owning verify row gi: the last r with rowoff[r] <= gi
+    // request owning verify row gi: the last r with rowoff[r] <= gi (shared-memory copy)
     int lo = 0, hi = p.R - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.rowoff[mid] <= gi) lo = mid; else hi = mid - 1;
+      if (s_rowoff[mid] <= gi) lo = mid; else hi = mid - 1;
     }
-    const int r = lo, j = gi - p.rowoff[r];
+    const int r = lo, j = gi - s_rowoff[r];
     const size_t trw = static_cast<size_t>(r) * (p.gamma + 1) + j;
     const float* row = p.T + trw * p.V;
     const int c0 = c * kVerifyChunk;
@@ -304,14 +308,27 @@ __global__ void __launch_bounds__(256) k4_accept(const VerifyArgs p) {
   }
 }
 
-__global__ void __launch_bounds__(256) k4_residual_sample(const VerifyArgs p) {
+__global__ void __launch_bounds__(256) k4_residual_sample(const __grid_constant__ CUtensorMap tm_slab,
+                                                          const VerifyArgs p) {
   __shared__ BlockFindScratch sc;
   __shared__ float s_redz[32];
   __shared__ float s_e[256];
   __shared__ float s_part[8][32];
+  __shared__ __align__(128) uint16_t s_slab[256 * kSubN];  // W2 columns of the chosen sub-tile, [rank][32]
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ int s_landed;
+  __shared__ volatile int s_no_abort;  // the slab wait's abort word: never set
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const uint32_t bar = smem_u32(&s_bar);
+  if (tid == 0) {
+    s_no_abort = 0;
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    prefetch_tensormap(&tm_slab);
+  }
+  __syncthreads();
   pdl_launch_dependents();
   pdl_wait();
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int i = blockIdx.x;
   if (i >= p.rej[p.R_pad]) return;
   const int r = p.rej[i];
@@ -343,22 +360,28 @@ __global__ void __launch_bounds__(256) k4_residual_sample(const VerifyArgs p) {
                                  2 * (te - tb), before_c, target,
                                  [&](int k) -> float { return frow[static_cast<size_t>(2 * tb + k) * p.R_pad].x; },
                                  &before_s, sc);
-  // recompute the 32 residual weights of that sub-tile: column = lane, rank split over warps
+  // recompute the 32 residual weights of that sub-tile: the W2 columns come in
+  // as one TMA box (rank x 32), each warp sums 32 rank rows for lane = column
+  const int v0 = sstar * kSubN;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.rank) * kSubN * 2u);
+    tma_load_2d(smem_u32(s_slab), &tm_slab, bar, v0, 0, policy_evict_normal());
+  }
   const int prev_raw = n == 0 ? p.anchors[r] : p.tokens[static_cast<size_t>(r) * p.gamma + n - 1];
   const int prev = (prev_raw >= 0 && prev_raw < p.V) ? prev_raw : 0;
   for (int k = tid; k < p.rank; k += 256) s_e[k] = bf16_at(p.W1 + static_cast<size_t>(prev) * p.rank + k);
+  if (tid == 0) s_landed = mbar_wait(bar, 0, &s_no_abort) ? 1 : 0;  // bounded; one waiter, shared verdict
   __syncthreads();
-  const int v = sstar * kSubN + lane;
-  const int per = p.rank / 8;
+  const int v = v0 + lane;
   float acc = 0.f;
-  if (v < p.V) {
-    const uint16_t* col = p.W2 + static_cast<size_t>(wid * per) * p.V + v;
-    uint16_t wv[32];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) wv[k] = k < per ? col[static_cast<size_t>(k) * p.V] : 0;
-#pragma unroll
-    for (int k = 0; k < 32; ++k)
-      if (k < per) acc = fmaf(s_e[wid * per + k], __uint_as_float(static_cast<uint32_t>(wv[k]) << 16), acc);
+  if (s_landed) {
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const int j = wid * 32 + k;
+      if (j < p.rank) acc = fmaf(s_e[j], __uint_as_float(static_cast<uint32_t>(s_slab[j * kSubN + lane]) << 16), acc);
+    }
+  } else if (tid == 0) {
+    report(p.status, DSPARK_STATUS_TIMEOUT);
   }
   s_part[wid][lane] = acc;
   __syncthreads();
@@ -382,7 +405,7 @@ __global__ void __launch_bounds__(256) k4_residual_sample(const VerifyArgs p) {
       const unsigned nz = __ballot_sync(0xffffffffu, w > 0.f);
       pick = nz ? 31 - __clz(nz) : 0;
     }
-    if (lane == 0) p.next_token[r] = min(max(sstar * kSubN + pick, 0), p.V - 1);
+    if (lane == 0) p.next_token[r] = min(max(v0 + pick, 0), p.V - 1);
   }
 }
 
@@ -431,7 +454,13 @@ int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint
   const long long cap = static_cast<long long>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (launch_pdl(k4_target_stats, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, true, p) != cudaSuccess)
+  const size_t rowoff_bytes = (static_cast<size_t>(R) + 1) * sizeof(int32_t);
+  if (rowoff_bytes > 48 * 1024 &&
+      cudaFuncSetAttribute(k4_target_stats, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(rowoff_bytes)) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (launch_pdl(k4_target_stats, dim3(static_cast<unsigned>(blocks)), dim3(256), rowoff_bytes, stream, true, p) !=
+      cudaSuccess)
     return DSPARK_ERR_CUDA;
   if (launch_pdl(k4_accept, dim3(R), dim3(256), 0, stream, true, p) != cudaSuccess)
     return DSPARK_ERR_CUDA;
@@ -449,7 +478,9 @@ int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint
   CUtensorMap tm_w2;
   if (encode_w2_map(&tm_w2, W2, V, rank) != DSPARK_OK) return DSPARK_ERR_CUDA;
   if (launch_residual_partials(tm_w2, a, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
-  if (launch_pdl(k4_residual_sample, dim3(R), dim3(256), 0, stream, true, p) != cudaSuccess)
+  CUtensorMap tm_slab;
+  if (encode_w2_slab_map(&tm_slab, W2, V, rank) != DSPARK_OK) return DSPARK_ERR_CUDA;
+  if (launch_pdl(k4_residual_sample, dim3(R), dim3(256), 0, stream, true, tm_slab, p) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }

@@ -16,6 +16,9 @@ constexpr int kTmemCols = 256;        // accumulators + the A operand (rank / 2 
 // W2 [rank, V] bf16 as a 2-D tensor; box 64 x rank, 128-byte swizzle (the
 // MN-major SW128 B-operand layout of the UMMA).
 int encode_w2_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank);
+// W2 again, box 32 x rank without swizzle: the 32 columns of one sub-tile as
+// [rank][32] (the samplers' recompute of a sub-tile's bias).
+int encode_w2_slab_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank);
 // U [R, gamma, V] fp32 as a 3-D tensor; box 68 x 1 x 128, no swizzle.
 int encode_u_map(CUtensorMap* tm, const float* U, int R, int gamma, int V);
 // Contiguous V-chunks per M-tile so that chunks x M-tiles fills the SMs once.
