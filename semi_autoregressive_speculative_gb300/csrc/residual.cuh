@@ -265,11 +265,23 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
       l2zd = p.logZd[static_cast<size_t>(rr.y) * p.gamma + rr.z] * 1.4426950408889634f;
     }
     float runS = 0.f;  // running sum of w over this warp's half of the chunk
+    // a warp with no rejected row in its lane quarter only keeps the rings moving
+    const bool warp_works = __any_sync(0xffffffffu, valid);
     for (int i = 0; i < ntile; ++i) {
       const int s = i % kStages, acc = i & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, (i >> 1) & 1, abort_flag))) {
         *abort_flag = 1;
         break;
+      }
+      if (!warp_works) {
+        if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_ufull + 8 * s, (i / kStages) & 1, abort_flag))) {
+          *abort_flag = 1;
+          break;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_uempty + 8 * s);
+        continue;
       }
       tc_fence_after_sync();
       float v[32];

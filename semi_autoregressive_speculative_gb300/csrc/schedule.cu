@@ -2,7 +2,7 @@
 // section "按负载决定验证多少").  One CTA of 1024 threads, everything in
 // shared memory, no host round trip:
 //   1. keys (a descending, j ascending, r ascending) packed into 64 bits and
-//      bitonic-sorted;
+//      bitonic-sorted (warp barriers for the passes inside a warp);
 //   2. a -> Q.40 fixed point and an integer inclusive scan: S_b is the same for
 //      every summation order;
 //   3. Theta(b) = (R + S_b 2^-40) * SPS[R + b] in fp64 for every b;
@@ -70,7 +70,10 @@ __global__ void __launch_bounds__(kSchedThreads)
   }
   for (int r = tid; r < R; r += kSchedThreads) cnt[r] = 0;
   __syncthreads();
-  // 2. bitonic sort, ascending
+  // 2. bitonic sort, ascending.  Thread t handles indices t + 1024 m, so a warp
+  // owns 32 consecutive indices of every block of 1024: passes whose partner
+  // distance is below 32 stay inside the warp and need only a warp barrier;
+  // the CTA barrier follows the wider passes and each merge size.
   for (int k = 2; k <= npow2; k <<= 1) {
     for (int jj = k >> 1; jj > 0; jj >>= 1) {
       for (int i = tid; i < npow2; i += kSchedThreads) {
@@ -81,8 +84,10 @@ __global__ void __launch_bounds__(kSchedThreads)
           if ((x > y) == up) { keys[i] = y; keys[ixj] = x; }
         }
       }
-      __syncthreads();
+      if (jj >= 32) __syncthreads(); else __syncwarp();
     }
+    // merges up to 32 wide never leave a warp; the next, wider one reads across warps
+    if (k >= 32) __syncthreads(); else __syncwarp();
   }
   // 3. fixed-point values and request ids in sorted order; S[0] = 0
   for (int i = tid; i < n; i += kSchedThreads) {

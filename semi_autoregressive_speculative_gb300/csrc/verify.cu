@@ -4,7 +4,7 @@
 //
 //  k4_prepare       one CTA: verify-row offsets (exclusive scan of lens + 1),
 //                   clears the rejection list.
-//  k4_target_stats  one warp per (verify row, 1024-column chunk; row owners from a
+//  k4_target_stats  one warp per (verify row, 2048-column chunk; row owners from a
 //                   shared-memory copy of the row offsets): softmax
 //                   partials of T / temperature (or max / argmax), and the
 //                   target logit at the drafted token.
@@ -124,9 +124,10 @@ __global__ void __launch_bounds__(256) k4_target_stats(const VerifyArgs p) {
     const float* row = p.T + trw * p.V;
     const int c0 = c * kVerifyChunk;
     const int ncol = min(kVerifyChunk, p.V - c0);
-    float t[32];
+    constexpr int kPer = kVerifyChunk / 32;  // values per lane (16-byte loads, all in flight)
+    float t[kPer];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < kPer / 4; ++k) {
       const int col = (k * 32 + lane) * 4;
       float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       if (col < ncol) v = __ldcs(reinterpret_cast<const float4*>(row + c0 + col));
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(256) k4_target_stats(const VerifyArgs p) {
       float mx = -INFINITY;
       int ix = 0x7fffffff;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
+      for (int k = 0; k < kPer; ++k) {
         const int col = c0 + (k >> 2) * 128 + lane * 4 + (k & 3);
         if (t[k] > mx || (t[k] == mx && col < ix)) { mx = t[k]; ix = col; }
       }
@@ -151,12 +152,12 @@ __global__ void __launch_bounds__(256) k4_target_stats(const VerifyArgs p) {
     } else {
       float mx = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) { t[k] *= p.scale; mx = fmaxf(mx, t[k]); }
+      for (int k = 0; k < kPer; ++k) { t[k] *= p.scale; mx = fmaxf(mx, t[k]); }
       mx = warp_max(mx);
       float s = 0.f;
       if (mx > -INFINITY) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) s += exp2f(t[k] - mx);
+        for (int k = 0; k < kPer; ++k) s += exp2f(t[k] - mx);
       }
       s = warp_sum(s);
       res = make_float2(mx, s);
@@ -209,7 +210,7 @@ __device__ __forceinline__ int row_argmax(const float2* st, int n_vc) {
 }
 
 // Inverse CDF of softmax(T_row * scale) with target u * Z, via the chunk
-// partials and a scan of the selected 1024-column chunk.
+// partials and a scan of the selected kVerifyChunk-column chunk.
 // Block-wide (256 threads); every thread gets the result.
 __device__ int sample_target_row(const VerifyArgs& p, size_t trw, float M, float Z, float u, BlockFindScratch& sc) {
   const float2* st = p.tstats + trw * p.n_vc;
