@@ -104,15 +104,23 @@ int dspark_markov_draft(const float *U, const uint16_t *W1, const uint16_t *W2,
  *     c[r,j] = sigma( sum_i w[i] h[r,j,i] + sum_i w[d+i] W1[x_{j-1}, i] ),  x_{-1} = anchor
  *     a[r,j] = fp32(a[r,j-1] * c[r,j]),  a[r,-1] = 1  (left to right)
  * No bias term; w = [w_h (d) ; w_e (rank)] follows the concatenation [h ; W1[x]].
+ * Sequential temperature scaling ("DSpark" §3.2, STS): when sts_temperature is
+ * given, the logit of position j is divided by t_j before the sigmoid,
+ *     c[r,j] = sigma( logit[r,j] / t_j ),
+ * with the t_j fitted offline, position after position, by a grid search that
+ * minimises the calibration error of a[., j] (python: sts.fit_sts).
  *   h        bf16 [R, gamma, d]   backbone hidden states
  *   W1       bf16 [V, rank]
  *   w        fp32 [d + rank]
+ *   sts_temperature fp32 [gamma]  device, or NULL for no scaling; a t_j that is not a
+ *                                 finite positive number is taken as 1 and raises
+ *                                 DSPARK_STATUS_NONFINITE
  *   anchors  int32 [R], tokens int32 [R, gamma] (only columns 0..gamma-2 are read)
  *   c, a     fp32 [R, gamma]      out
  * Sizes: R >= 0, 1 <= gamma <= 64, d >= 1, rank >= 1.
  */
 int dspark_confidence(const uint16_t *h, const uint16_t *W1, const float *w,
-                      const int32_t *anchors, const int32_t *tokens, int R, int gamma, int d,
+                      const float *sts_temperature, const int32_t *anchors, const int32_t *tokens, int R, int gamma, int d,
                       int rank, int V, float *c, float *a, void *workspace, size_t workspace_bytes,
                       void *stream);
 

@@ -56,7 +56,7 @@ def lib() -> ctypes.CDLL:
             "oracle_draft_logits_f32": (None, [P, P, P, I32, I, I, P]),
             "oracle_target_probs": (D, [P, I, F, P]),
             "oracle_draft_request": (I, [P, P, P, I32, I, I, I, F, U64, U64, U64, P, P, P]),
-            "oracle_confidence_request": (I, [P, P, P, I32, P, I, I, I, I, P, P]),
+            "oracle_confidence_request": (I, [P, P, P, I32, P, I, I, I, I, P, P, P]),
             "oracle_survival": (None, [P, I, P]),
             "oracle_schedule": (I, [P, I, I, P, I, I, I, P, P, P, P, P]),
             "oracle_verify_request_u": (I, [P, P, P, P, I32, P, I, I, I, I, F, P, P, P, P]),
@@ -168,7 +168,10 @@ def draft(U, W1, W2, anchors, temperature: float, seed: int, rnd: int, request_i
 
 
 # ---------------------------------------------------------------- confidence
-def confidence(h, W1, w, anchors, tokens):
+def confidence(h, W1, w, anchors, tokens, sts_temperature=None):
+    """c, a of every request; sts_temperature: per-position temperatures
+    [gamma] that divide the confidence logits (None: no scaling)."""
+    sts = None if sts_temperature is None else _c(sts_temperature, np.float32)
     h = _c(h, np.uint16)
     W1 = _c(W1, np.uint16)
     w = _c(w, np.float32)
@@ -181,7 +184,8 @@ def confidence(h, W1, w, anchors, tokens):
         ci = np.zeros(gamma, np.float32)
         ai = np.zeros(gamma, np.float32)
         rc = lib().oracle_confidence_request(_p(h[i]), _p(W1), _p(w), int(anchors[i]),
-                                             _p(tokens[i]), gamma, d, rank, V, _p(ci), _p(ai))
+                                             _p(tokens[i]), gamma, d, rank, V,
+                                             None if sts is None else _p(sts), _p(ci), _p(ai))
         _check(rc, "confidence")
         c[i], a[i] = ci, ai
     return c, a

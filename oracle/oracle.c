@@ -244,18 +244,23 @@ void oracle_survival(const float *c, int gamma, float *a)
     }
 }
 
+/* [DSpark §3.2, STS]: with sequential temperature scaling the confidence of
+ * position j is sigma(s_j / t_j) for per-position temperatures t_j > 0
+ * (sts_temp == NULL: no scaling). */
 int oracle_confidence_request(const uint16_t *h_r, const uint16_t *W1, const float *w,
                               int32_t anchor, const int32_t *tokens, int gamma, int d, int rank,
-                              int V, float *c, float *a)
+                              int V, const float *sts_temp, float *c, float *a)
 {
     for (int j = 0; j < gamma; ++j) {
         int32_t prev = (j == 0) ? anchor : tokens[j - 1];
         if (prev < 0 || prev >= V) return ORACLE_ERR_ARG;
+        if (sts_temp && !(sts_temp[j] > 0.0f && sts_temp[j] <= 3.4e38f)) return ORACLE_ERR_ARG;
         double s = 0.0;
         const uint16_t *hj = h_r + (size_t)j * (size_t)d;
         for (int i = 0; i < d; ++i) s += (double)w[i] * bf16_value(hj[i]);
         const uint16_t *e = W1 + (size_t)prev * (size_t)rank;
         for (int i = 0; i < rank; ++i) s += (double)w[d + i] * bf16_value(e[i]);
+        if (sts_temp) s /= (double)sts_temp[j];
         c[j] = (float)(1.0 / (1.0 + exp(-s)));
     }
     oracle_survival(c, gamma, a);

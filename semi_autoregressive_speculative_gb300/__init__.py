@@ -56,7 +56,7 @@ def lib() -> ctypes.CDLL:
         L.dspark_markov_draft.restype = I
         L.dspark_markov_draft.argtypes = [P, P, P, P, I, I, I, I, F, U64, U32, P, P, P, P, SZ, P]
         L.dspark_confidence.restype = I
-        L.dspark_confidence.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, P, SZ, P]
+        L.dspark_confidence.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, SZ, P]
         L.dspark_schedule.restype = I
         L.dspark_schedule.argtypes = [P, I, I, P, I, I, I, P, P, P, P, P, SZ, P]
         L.dspark_verify.restype = I
@@ -116,11 +116,13 @@ def dspark_markov_draft(U, W1, W2, anchors, temperature, seed, round_, tokens, p
         _stream(stream)))
 
 
-def dspark_confidence(h, W1, w, anchors, tokens, c, a, workspace, stream=None) -> None:
+def dspark_confidence(h, W1, w, anchors, tokens, c, a, workspace, stream=None, sts_temperature=None) -> None:
     R, gamma, d = h.shape
     V, rank = W1.shape
+    if sts_temperature is not None and tuple(sts_temperature.shape) != (gamma,):
+        raise ValueError(f"sts_temperature must have shape ({gamma},), got {tuple(sts_temperature.shape)}")
     _check("dspark_confidence", lib().dspark_confidence(
-        _ptr(h), _ptr(W1), _ptr(w), _ptr(anchors), _ptr(tokens), R, gamma, d, rank, V, _ptr(c), _ptr(a),
+        _ptr(h), _ptr(W1), _ptr(w), _ptr(sts_temperature), _ptr(anchors), _ptr(tokens), R, gamma, d, rank, V, _ptr(c), _ptr(a),
         _ptr(workspace), _nbytes(workspace), _stream(stream)))
 
 

@@ -11,9 +11,9 @@ namespace dspark {
 int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors, int R,
                         int gamma, int V, int rank, float temperature, uint64_t seed, uint32_t round,
                         int32_t* tokens, float* pd_tok, float* logZ, void* workspace, cudaStream_t stream);
-int launch_confidence(const uint16_t* h, const uint16_t* W1, const float* w, const int32_t* anchors,
-                      const int32_t* tokens, int R, int gamma, int d, int rank, int V, float* c, float* a,
-                      int32_t* status, cudaStream_t stream);
+int launch_confidence(const uint16_t* h, const uint16_t* W1, const float* w, const float* sts_t,
+                      const int32_t* anchors, const int32_t* tokens, int R, int gamma, int d, int rank, int V,
+                      float* c, float* a, int32_t* status, cudaStream_t stream);
 int launch_schedule(const float* a, int R, int gamma, const double* sps, int mode, int budget_K, int32_t* lens,
                     int32_t* total_b, int32_t* argmax_b, double* theta, int32_t* status, cudaStream_t stream);
 int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors,
@@ -71,16 +71,16 @@ int dspark_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
                              workspace, static_cast<cudaStream_t>(stream));
 }
 
-int dspark_confidence(const uint16_t* h, const uint16_t* W1, const float* w, const int32_t* anchors,
-                      const int32_t* tokens, int R, int gamma, int d, int rank, int V, float* c, float* a,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+int dspark_confidence(const uint16_t* h, const uint16_t* W1, const float* w, const float* sts_temperature,
+                      const int32_t* anchors, const int32_t* tokens, int R, int gamma, int d, int rank, int V,
+                      float* c, float* a, void* workspace, size_t workspace_bytes, void* stream) {
   if (R < 0 || gamma < 1 || d < 1 || rank < 1 || V < 1) return DSPARK_ERR_INVALID_ARG;
   if (gamma > kMaxGamma) return DSPARK_ERR_UNSUPPORTED_SHAPE;
   if (R == 0) return DSPARK_OK;
   if (!h || !W1 || !w || !anchors || !tokens || !c || !a || !workspace) return DSPARK_ERR_INVALID_ARG;
   if (workspace_bytes < sizeof(int32_t)) return DSPARK_ERR_INVALID_ARG;
-  return launch_confidence(h, W1, w, anchors, tokens, R, gamma, d, rank, V, c, a, static_cast<int32_t*>(workspace),
-                           static_cast<cudaStream_t>(stream));
+  return launch_confidence(h, W1, w, sts_temperature, anchors, tokens, R, gamma, d, rank, V, c, a,
+                           static_cast<int32_t*>(workspace), static_cast<cudaStream_t>(stream));
 }
 
 int dspark_schedule(const float* a, int R, int gamma, const double* sps, int sps_len, int mode, int budget_K,

@@ -70,9 +70,9 @@ class DeviceRound:
         dspark_markov_draft(self.U, self.W1, self.W2, self.anchors, temperature, seed, rnd, self.tokens, self.pd,
                             self.logZ, self.workspace)
 
-    def confidence(self, tokens=None):
+    def confidence(self, tokens=None, sts_temperature=None):
         dspark_confidence(self.h, self.W1, self.w, self.anchors, self.tokens if tokens is None else tokens,
-                          self.c, self.a, self.workspace)
+                          self.c, self.a, self.workspace, sts_temperature=sts_temperature)
 
     def schedule(self, mode: int, budget_K: int = 0, a=None):
         dspark_schedule(self.a if a is None else a, self.sps, mode, budget_K, self.lens, self.sched_out[0:1],

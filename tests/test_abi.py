@@ -76,9 +76,12 @@ def test_schedule_validation(L):
 
 
 def test_confidence_and_verify_validation(L):
-    assert L.dspark_confidence(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 7, 0, 256, 4096, FAKE, FAKE, FAKE, 4, None) == -1
-    assert L.dspark_confidence(0, FAKE, FAKE, FAKE, FAKE, 4, 7, 64, 256, 4096, FAKE, FAKE, FAKE, 4, None) == -1
-    assert L.dspark_confidence(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 7, 64, 256, 4096, FAKE, FAKE, FAKE, 4, None) == 0
+    def conf(h=FAKE, R=4, d=64, sts=None):
+        return L.dspark_confidence(h, FAKE, FAKE, sts, FAKE, FAKE, R, 7, d, 256, 4096, FAKE, FAKE, FAKE, 4, None)
+    assert conf(d=0) == -1
+    assert conf(h=0) == -1
+    assert conf(R=0) == 0
+    assert conf(R=0, sts=FAKE) == 0
 
     def verify(T=FAKE, V=4096, temp=1.0, wsb=1 << 30):
         return L.dspark_verify(T, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 7, V, 256, temp, 0, 0,

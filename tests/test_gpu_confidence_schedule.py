@@ -42,6 +42,43 @@ def test_confidence(wl):
     assert dr.status() == 0
 
 
+@pytest.mark.parametrize("wl", [
+    TINY,
+    synth.scaled(TINY, R=3, gamma=33, V=64, d=8, rank=64, name="g33"),
+    synth.WORKLOADS["r128_g16_v151936"],
+], ids=lambda w: w.name)
+def test_confidence_sts(wl):
+    # sequential temperature scaling ("DSpark" §3.2): c_j = sigma(logit_j / t_j)
+    dr, inp = device_round(wl)
+    W1, _, w = weights(wl)
+    tok = _tokens(wl, 1)
+    t = np.random.default_rng([wl.seed, 78]).uniform(0.3, 4.0, wl.gamma).astype(np.float32)
+    t[0] = 1.0
+    dr.tokens.copy_(torch.from_numpy(tok))
+    dr.confidence(sts_temperature=torch.from_numpy(t).cuda())
+    c_g, a_g = host(dr.c), host(dr.a)
+    c_o, a_o = oracle.confidence(inp.h, W1, w, inp.anchors, tok, sts_temperature=t)
+    assert np.max(np.abs(c_g - c_o)) <= PROB_TOL
+    assert np.max(np.abs(a_g - a_o)) <= PROB_TOL
+    assert dr.status() == 0
+    # unit temperatures give the unscaled head exactly
+    dr.confidence(sts_temperature=torch.ones(wl.gamma, device="cuda"))
+    c_1 = host(dr.c)
+    dr.confidence()
+    assert np.array_equal(c_1, host(dr.c))
+
+
+def test_confidence_sts_bad_temperature_is_reported():
+    dr, _ = device_round(TINY)
+    t = torch.ones(TINY.gamma, device="cuda")
+    t[2] = 0.0
+    dr.confidence(sts_temperature=t)
+    torch.cuda.synchronize()
+    assert dr.status() & 1  # DSPARK_STATUS_NONFINITE
+    with pytest.raises(ValueError):
+        dr.confidence(sts_temperature=torch.ones(TINY.gamma + 1, device="cuda"))
+
+
 def _schedule_both(dr, a, sps, mode, K=0):
     dr.sps[: len(sps)].copy_(torch.from_numpy(sps))
     a_dev = torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()

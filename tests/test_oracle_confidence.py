@@ -75,3 +75,27 @@ def test_tau_is_expected_emitted_tokens(orc):
         emitted[rnd] = na[0] + 1
     se = emitted.std() / np.sqrt(n)
     assert abs(emitted.mean() - tau) < 4 * se
+
+
+def test_sts_temperatures_divide_the_logits(orc):
+    # sequential temperature scaling ("DSpark" page §3.2): c_j = sigma(s_j / t_j)
+    from scipy import special
+    rng = np.random.default_rng(3)
+    V, rank, d, gamma, n = 40, 16, 24, 5, 3
+    W1 = synth.to_bf16_bits(rng.standard_normal((V, rank)).astype(np.float32) * 0.5)
+    h = synth.to_bf16_bits(rng.standard_normal((n, gamma, d)).astype(np.float32))
+    w = (rng.standard_normal(d + rank) * 0.3).astype(np.float32)
+    anchors = rng.integers(0, V, n).astype(np.int32)
+    tokens = rng.integers(0, V, (n, gamma)).astype(np.int32)
+    t = np.array([1.0, 0.5, 2.0, 3.0, 0.25], np.float32)
+    c1, _ = orc.confidence(h, W1, w, anchors, tokens)
+    cu, au = orc.confidence(h, W1, w, anchors, tokens, sts_temperature=np.ones(gamma, np.float32))
+    np.testing.assert_array_equal(cu, c1)  # unit temperatures change nothing
+    ct, at = orc.confidence(h, W1, w, anchors, tokens, sts_temperature=t)
+    logit = np.log(c1.astype(np.float64)) - np.log1p(-c1.astype(np.float64))
+    np.testing.assert_allclose(ct, special.expit(logit / t.astype(np.float64)), atol=2e-7)
+    np.testing.assert_array_equal(at, np.cumprod(ct, axis=1, dtype=np.float32))
+    # t > 1 pulls a confidence towards 1/2, t < 1 away from it
+    hot, cold = t > 1, t < 1
+    assert np.all(np.abs(ct[:, hot] - 0.5) <= np.abs(c1[:, hot] - 0.5) + 1e-7)
+    assert np.all(np.abs(ct[:, cold] - 0.5) >= np.abs(c1[:, cold] - 0.5) - 1e-7)
