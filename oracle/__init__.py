@@ -63,6 +63,7 @@ def lib() -> ctypes.CDLL:
             "oracle_verify_request": (I, [P, P, P, P, I32, P, I, I, I, I, F, U64, U64, U64, P, P]),
             "oracle_verify_position": (I, [P, P, I, I32, D, D, P, P]),
             "oracle_overlap": (D, [P, P, I]),
+            "oracle_c_star_request": (I, [P, P, P, P, I32, P, I, I, I, I, F, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -283,3 +284,23 @@ def overlap(pd, pt) -> float:
     pd = _c(pd, np.float64)
     pt = _c(pt, np.float64)
     return lib().oracle_overlap(_p(pd), _p(pt), pd.shape[0])
+
+
+def c_star(T, U, W1, W2, anchors, tokens, lens, temperature: float) -> np.ndarray:
+    """Analytic acceptance c* [n, gamma] (fp64) of every position j <= lens[i]
+    with j < gamma; NaN elsewhere."""
+    T = _c(T, np.float32)
+    U = _c(U, np.float32)
+    W1 = _c(W1, np.uint16)
+    W2 = _c(W2, np.uint16)
+    tokens = _c(tokens, np.int32)
+    n, gamma, V = U.shape
+    out = np.empty((n, gamma), np.float64)
+    for i in range(n):
+        row = np.empty(gamma, np.float64)
+        rc = lib().oracle_c_star_request(_p(T[i]), _p(U[i]), _p(W1), _p(W2), int(anchors[i]),
+                                         _p(tokens[i]), int(lens[i]), gamma, V, W1.shape[1],
+                                         float(temperature), _p(row))
+        _check(rc, "c_star")
+        out[i] = row
+    return out

@@ -449,3 +449,36 @@ double oracle_overlap(const double *pd, const double *pt, int V)
     for (int v = 0; v < V; ++v) l1 += fabs(pd[v] - pt[v]);
     return 1.0 - 0.5 * l1;
 }
+
+/* [DSpark §3.1, eq. c_k*] over the rows one verification reads: for every
+ * position j <= len that has a draft distribution (j < gamma), c*[j] is the
+ * overlap of the draft distribution at j (conditioned on x_{j-1}, x_{-1} =
+ * anchor) with the target distribution of row j; positions j > len get NaN.
+ * T == 0: both distributions are point masses, the draft's at its token x_j
+ * and the target's at the first argmax of row j, so c*[j] is 1 or 0. */
+int oracle_c_star_request(const float *T_r, const float *U_r, const uint16_t *W1,
+                          const uint16_t *W2, int32_t anchor, const int32_t *tokens, int len,
+                          int gamma, int V, int rank, float temperature, double *c_star)
+{
+    if (len < 0 || len > gamma || V <= 0) return ORACLE_ERR_ARG;
+    for (int j = 0; j < gamma; ++j) c_star[j] = NAN;
+    int last = len < gamma ? len : gamma - 1;
+    if (temperature <= 0.0f) {
+        for (int j = 0; j <= last; ++j)
+            c_star[j] = tokens[j] == argmax_f32(T_r + (size_t)j * V, V) ? 1.0 : 0.0;
+        return ORACLE_OK;
+    }
+    double *pt = (double *)malloc(sizeof(double) * (size_t)V);
+    double *pd = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!pt || !pd) { free(pt); free(pd); return ORACLE_ERR_MEM; }
+    for (int j = 0; j <= last; ++j) {
+        int32_t prev = (j == 0) ? anchor : tokens[j - 1];
+        if (prev < 0 || prev >= V) { free(pt); free(pd); return ORACLE_ERR_ARG; }
+        oracle_target_probs(T_r + (size_t)j * V, V, temperature, pt);
+        oracle_draft_probs(U_r + (size_t)j * V, W1, W2, prev, V, rank, temperature, pd);
+        c_star[j] = oracle_overlap(pd, pt, V);
+    }
+    free(pt);
+    free(pd);
+    return ORACLE_OK;
+}

@@ -158,3 +158,61 @@ def test_greedy_special_case(orc):
         na, nx = orc.verify(T[None], U[None], W1, W2, [0], np.array([toks], np.int32), [length],
                             0.0, seed=0, rnd=0)
         assert (na[0], nx[0]) == (n_acc, nxt)
+
+
+def test_c_star_is_the_acceptance_probability(orc):
+    # c*_j ("DSpark" §3.1, eq. c_k*) is the chance that verification accepts
+    # position j given an accepted prefix: E_{x ~ p_d}[min(1, p_t(x) / p_d(x))].
+    # Measured here on the verifier itself, sweeping its accept uniform over a
+    # fine grid for every candidate x at position j; the prefix is accepted by
+    # giving it u = 0.
+    rng = np.random.default_rng(11)
+    V, rank, gamma, N = 5, 4, 3, 400
+    W1, W2, U = _tiny(rng, V, rank, gamma)
+    T = (rng.standard_normal((gamma + 1, V)) * 1.3).astype(np.float32)
+    anchor, temp = 1, 0.8
+    prefix = np.array([3, 0, 0], np.int32)
+    cs = orc.c_star(T[None], U[None], W1, W2, [anchor], prefix[None], [gamma], temp)[0]
+    grid = (np.arange(N) + 0.5) / N
+    for j in range(gamma):
+        prev = anchor if j == 0 else int(prefix[j - 1])
+        pd, _ = orc.draft_probs(U[j], W1, W2, prev, temp)
+        expect = 0.0
+        for x in range(V):
+            toks = prefix.copy()
+            toks[j] = x
+            acc = 0
+            for ua in grid:
+                u_acc = np.zeros(gamma)
+                u_acc[j] = ua
+                na, _ = orc.verify_request_u(T, U, W1, W2, anchor, toks, j + 1, temp, u_acc, np.full(gamma + 1, 0.5))
+                acc += na == j + 1
+            expect += pd[x] * acc / N
+        assert abs(cs[j] - expect) <= 1.0 / N
+
+
+def test_c_star_rows_identity_and_greedy(orc):
+    rng = np.random.default_rng(12)
+    V, rank, gamma = 7, 4, 4
+    W1, W2, U = _tiny(rng, V, rank, gamma)
+    anchor = 2
+    toks = np.array([[1, 6, 0, 3]], np.int32)
+    # target rows equal to the draft logits: the distributions coincide, c* = 1
+    T = np.empty((gamma + 1, V), np.float32)
+    for j in range(gamma):
+        prev = anchor if j == 0 else int(toks[0, j - 1])
+        T[j] = orc.draft_logits_f32(U[j], W1, W2, prev)
+    T[gamma] = 0.0
+    for length in range(gamma + 1):
+        cs = orc.c_star(T[None], U[None], W1, W2, [anchor], toks, [length], 1.3)[0]
+        last = min(length, gamma - 1)
+        np.testing.assert_allclose(cs[: last + 1], 1.0, atol=1e-6)
+        assert np.all(np.isnan(cs[last + 1:]))  # positions past the verified rows
+    # greedy: 1 where the drafted token is the target's first argmax, else 0
+    Tg = rng.standard_normal((gamma + 1, V)).astype(np.float32)
+    Tg[1, 6] = Tg[1].max() + 1.0
+    Tg[2, 4] = Tg[2, 0] = Tg[2].max() + 1.0  # tie: the argmax is 0
+    cs = orc.c_star(Tg[None], U[None], W1, W2, [anchor], toks, [3], 0.0)[0]
+    expect = [float(toks[0, j] == int(np.argmax(Tg[j]))) for j in range(4)]
+    np.testing.assert_array_equal(cs, expect)
+    assert cs[1] == 1.0 and cs[2] == 1.0
