@@ -298,6 +298,11 @@ def run_gpu(args):
     with torch.cuda.graph(round_graph, stream=stream):
         for f in calls:
             f()
+    # verify with the optional analytic acceptance c*: reported beside the
+    # breakdown, not part of the timed round
+    cstar_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cstar_graph, stream=stream):
+        dr.verify(temp, seed, rnd, c_star=True)
     # draft: one persistent kernel; confidence 1; schedule 1; verify 3 (greedy) or 5
     launches_per_step = 1 + 1 + 1 + (3 if temp == 0 else 5)
 
@@ -322,7 +327,7 @@ def run_gpu(args):
     n_bd = max(3, min(args.steps, 50))
     per_call = []
     with torch.cuda.stream(stream):
-        for g in graphs:
+        for g in graphs + [cstar_graph]:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for _ in range(n_bd):
@@ -350,6 +355,10 @@ def run_gpu(args):
     round_bytes = (draft_bytes + R * g * d * 2 + R * g * rk * 2 + rows_read * V * 4 + n_rej * V * 8 +
                    (rk * V * 2 if n_rej else 0))
     round_gbs = round_bytes / (t_max / args.steps) / 1e9
+    # c* re-reads the U and T rows of every verified position with a draft
+    # distribution (W2 once) on top of the target-row statistics
+    cstar_rows = int(np.minimum(lens_h + 1, g).sum()) if temp > 0 else 0
+    cstar_bytes = rows_read * V * 4 + cstar_rows * V * 8 + (rk * V * 2 if cstar_rows else 0)
     digest = kernel_digest()
     traffic = NCU_DRAFT_TRAFFIC["bytes_per_call"] if NCU_DRAFT_TRAFFIC["digest"] == digest else None
 
@@ -409,6 +418,9 @@ def run_gpu(args):
                          "algorithmic_bytes": draft_bytes, "ms_per_call": per_call[0]},
             "breakdown_ms": {"draft": per_call[0], "confidence": per_call[1], "schedule": per_call[2],
                              "verify": per_call[3]},
+            "verify_c_star": {"ms": per_call[4], "rows": cstar_rows, "algorithmic_bytes": cstar_bytes,
+                              "achieved": cstar_bytes / (per_call[4] / 1e3) / 1e9, "unit": "GB/s",
+                              "note": "dspark_verify with the optional c* output; outside the timed round"},
             "round": {"algorithmic_bytes": round_bytes, "achieved": round_gbs, "unit": "GB/s",
                       "frac": round_gbs / peak, "verified_rows": rows_read, "rejected_rows": n_rej,
                       "admitted_positions": int(lens_h.sum())},

@@ -163,6 +163,16 @@ int dspark_schedule(const float *a, int R, int gamma, const double *sps, int sps
  *   lens     int32 [R]            verify lengths (from dspark_schedule)
  *   n_accept int32 [R]            out: accepted drafts
  *   next_token int32 [R]          out: correction or bonus token
+ *   c_star   fp32 [R, gamma]      optional out (NULL: not computed, no extra work): the
+ *                                 analytic acceptance ("DSpark" §3.1, eq. c_k*)
+ *                                     c*[r,j] = 1 - 1/2 || p_d - p_t ||_1
+ *                                 of every position j <= lens[r] (j < gamma), with p_d the
+ *                                 draft distribution at j (conditioned on x_{j-1}) and p_t
+ *                                 that of target row j; NaN for j > lens[r].  T == 0: both
+ *                                 are point masses, c* = 1 if x_j == argmax T[r,j,:], else 0.
+ *                                 With T > 0 the residual pass then covers every such row
+ *                                 (it re-reads their U and T rows) instead of the rejected
+ *                                 rows only.
  * Only rows 0..lens[r] of each request are read.
  * Sizes: as dspark_markov_draft, and R <= 32768.
  */
@@ -170,7 +180,8 @@ int dspark_verify(const float *T, const float *U, const uint16_t *W1, const uint
                   const int32_t *anchors, const int32_t *tokens, const float *pd_tok,
                   const float *logZ, const int32_t *lens, int R, int gamma, int V, int rank,
                   float temperature, uint64_t seed, uint32_t round, int32_t *n_accept,
-                  int32_t *next_token, void *workspace, size_t workspace_bytes, void *stream);
+                  int32_t *next_token, float *c_star, void *workspace, size_t workspace_bytes,
+                  void *stream);
 
 /*
  * dspark_markov_draft_noalloc — the Markov-head draft of dspark_markov_draft

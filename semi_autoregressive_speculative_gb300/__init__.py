@@ -60,7 +60,7 @@ def lib() -> ctypes.CDLL:
         L.dspark_schedule.restype = I
         L.dspark_schedule.argtypes = [P, I, I, P, I, I, I, P, P, P, P, P, SZ, P]
         L.dspark_verify.restype = I
-        L.dspark_verify.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, U64, U32, P, P, P, SZ, P]
+        L.dspark_verify.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, U64, U32, P, P, P, P, SZ, P]
         L.dspark_markov_draft_noalloc.restype = I
         L.dspark_markov_draft_noalloc.argtypes = [P, P, P, P, I, I, I, I, F, U64, U32, P, P, P, P, P]
         _lib = L
@@ -134,13 +134,16 @@ def dspark_schedule(a, sps, mode, budget_K, lens, total_b, argmax_b, theta, work
 
 
 def dspark_verify(T, U, W1, W2, anchors, tokens, pd_tok, logZ, lens, temperature, seed, round_, n_accept,
-                  next_token, workspace, stream=None) -> None:
+                  next_token, workspace, stream=None, c_star=None) -> None:
+    """`c_star`: optional fp32 [R, gamma] device tensor for the analytic acceptance."""
     R, gamma, V = U.shape
     rank = W1.shape[1]
+    if c_star is not None and tuple(c_star.shape) != (R, gamma):
+        raise ValueError(f"c_star must have shape ({R}, {gamma}), got {tuple(c_star.shape)}")
     _check("dspark_verify", lib().dspark_verify(
         _ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _ptr(anchors), _ptr(tokens), _ptr(pd_tok), _ptr(logZ),
         _ptr(lens), R, gamma, V, rank, float(temperature), int(seed), int(round_), _ptr(n_accept),
-        _ptr(next_token), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+        _ptr(next_token), _ptr(c_star), _ptr(workspace), _nbytes(workspace), _stream(stream)))
 
 
 def dspark_markov_draft_noalloc(U, W1, W2, anchors, temperature, seed, round_, tokens, pd_tok, logZ, status=None,

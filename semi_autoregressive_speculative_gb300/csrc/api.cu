@@ -19,7 +19,7 @@ int launch_schedule(const float* a, int R, int gamma, const double* sps, int mod
 int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors,
                   const int32_t* tokens, const float* pd_tok, const float* logZ, const int32_t* lens, int R, int gamma,
                   int V, int rank, float temperature, uint64_t seed, uint32_t round, int32_t* n_accept,
-                  int32_t* next_token, void* workspace, cudaStream_t stream);
+                  int32_t* next_token, float* c_star, void* workspace, cudaStream_t stream);
 
 int sm_count() {
   static int count[64] = {0};
@@ -98,7 +98,7 @@ int dspark_schedule(const float* a, int R, int gamma, const double* sps, int sps
 int dspark_verify(const float* T, const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors,
                   const int32_t* tokens, const float* pd_tok, const float* logZ, const int32_t* lens, int R, int gamma,
                   int V, int rank, float temperature, uint64_t seed, uint32_t round, int32_t* n_accept,
-                  int32_t* next_token, void* workspace, size_t workspace_bytes, void* stream) {
+                  int32_t* next_token, float* c_star, void* workspace, size_t workspace_bytes, void* stream) {
   if (R < 0 || gamma < 1 || V < 8 || rank < 1 || !finite_nonneg(temperature)) return DSPARK_ERR_INVALID_ARG;
   if (gamma > kMaxGamma || V % 8 != 0 || !rank_ok(rank) || R > kMaxVerifyR) return DSPARK_ERR_UNSUPPORTED_SHAPE;
   if (R == 0) return DSPARK_OK;
@@ -110,7 +110,7 @@ int dspark_verify(const float* T, const float* U, const uint16_t* W1, const uint
     return DSPARK_ERR_INVALID_ARG;
   if (workspace_bytes < workspace_layout(R, gamma, V).total) return DSPARK_ERR_INVALID_ARG;
   return launch_verify(T, U, W1, W2, anchors, tokens, pd_tok, logZ, lens, R, gamma, V, rank, temperature, seed, round,
-                       n_accept, next_token, workspace, static_cast<cudaStream_t>(stream));
+                       n_accept, next_token, c_star, workspace, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -1,5 +1,7 @@
-// Tensor-core residual pass of verify (included by verify.cu only): for the rejected request rows (up to
-// 128 per M-tile), each with the previous token x_i of its rejected position,
+// Tensor-core residual pass of verify (included by verify.cu only): for up to
+// 128 rows per M-tile — the rejected positions, or, when the analytic
+// acceptance c* is wanted, every verify row that has a draft position — each
+// with the previous token x_i of its position,
 // the draft bias row W1[x_i] . W2 ("DSpark" §2.3, B = W1 W2) is re-formed 64
 // vocabulary columns at a time by a tcgen05 UMMA (M = 128 rows, N = 64,
 // K = rank, bf16 x bf16 -> fp32 in tensor memory) and reduced on the fly —
@@ -8,6 +10,9 @@
 //   p_d = exp2(y - log2 Z_d) with y = (bias + U) * log2(e)/T,
 //   p_t = exp2(T_row * log2(e)/T - M_t) / Z_t,   w = max(0, p_t - p_d),
 //   per 32-column sub-tile and per CTA chunk: sum of w.
+//
+// Summed over the vocabulary, w gives 1 - c* for that row ("DSpark" §3.1,
+// eq. c_k*: sum max(0, p_t - p_d) = 1/2 ||p_d - p_t||_1).
 //
 // One CTA per (contiguous V-chunk, M-tile), 10 warps:
 //   warp 0     producer: W2 tiles by TMA (MN-major, 128B-swizzled) into a
@@ -39,10 +44,12 @@ struct ResidualArgs {
   const float* T;          // [R, gamma+1, V]
   const int32_t* rej;      // [R_pad + 1]: rejected requests; rej[R_pad] = their number
   const int32_t* n_acc;    // [R] rejected position of each request
+  const int32_t* rowoff;   // [R+1] verify row offsets; non-null: one row per verify row with a draft position
   const float4* trow;      // [R*(gamma+1)] (max, Z) of each target row, base-2 units
   const float* logZd;      // [R, gamma] draft log-normaliser (natural log)
-  float2* coarse;          // [R_pad][n_chunks]: x = sum of w over the chunk
-  float2* fine;            // [2 * n_tiles][R_pad]: x = sum of w over the 32-column sub-tile
+  float2* coarse;          // [row][n_chunks]: x = sum of w over the chunk
+  float2* fine;            // [2 * n_tiles][R_pad]: x = sum of w over the 32-column sub-tile, rejected
+                           // rows only (column = rejection slot, or request when rowoff is set)
   int32_t* status;
   int R, R_pad, gamma, V, rank;
   int n_tiles, n_chunks, n_mtiles;
@@ -59,7 +66,7 @@ __host__ __device__ inline ResidualSmem residual_smem_plan(int rank) {
   for (int i = 0; i < kStages; ++i) { s.u[i] = off; off += kMTile * kUStride; } // 128 rows x 64 fp32, padded rows
   s.half = off; off += kMTile * 8;   // second-half chunk partials
   s.bars = off; off += 256;          // mbarriers, tmem slot, abort flag
-  s.rows = off; off += kMTile * 16;  // residual rows: token, request, position
+  s.rows = off; off += kMTile * 16;  // residual rows: token, request, position, fine column
   s.total = off + 1024;              // alignment slack
   return s;
 }
@@ -78,7 +85,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
   const int r0 = mtile * kMTile;
 
   pdl_wait();
-  const int nrows = p.rej[p.R_pad];
+  const int nrows = p.rowoff != nullptr ? p.rowoff[p.R] : p.rej[p.R_pad];
   if (r0 >= nrows) return;  // no residual rows for this M-tile
   const int rows_valid = min(kMTile, nrows - r0);
   const int t_begin = static_cast<int>((static_cast<long long>(chunk) * p.n_tiles) / p.n_chunks);
@@ -93,7 +100,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
   const uint32_t bar_tempty = bar_tfull + 16;          // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + plan.bars + 32 * kStages + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + plan.bars + 32 * kStages + 36);
-  int4* s_rows = reinterpret_cast<int4*>(gbase + plan.rows);  // (token, request, position, -)
+  int4* s_rows = reinterpret_cast<int4*>(gbase + plan.rows);  // (token, request, position, fine column)
   float2* s_half = reinterpret_cast<float2*>(gbase + plan.half);
 
   if (threadIdx.x == 0) {
@@ -115,24 +122,45 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  // residual rows: request, rejected position, previous token
+  // residual rows: previous token, request, position, fine-partials column
+  // (-1: none); a row with token -1 is idle (a bonus row j == gamma, which has
+  // no draft distribution, or past the last row)
+  int live = 0;
   if (threadIdx.x < kMTile) {
     const int m = threadIdx.x;
-    int4 row = make_int4(-1, 0, 0, 0);
+    int4 row = make_int4(-1, 0, 0, -1);
     if (m < rows_valid) {
-      const int req = p.rej[r0 + m];
-      const int n = p.n_acc[req];
-      int tok = n == 0 ? p.anchors[req] : p.tokens[static_cast<size_t>(req) * p.gamma + n - 1];
-      if (tok < 0 || tok >= p.V) {
-        report(p.status, DSPARK_STATUS_BAD_TOKEN);
-        tok = 0;
+      int req, n, fcol;
+      if (p.rowoff != nullptr) {
+        const int gi = r0 + m;
+        int lo = 0, hi = p.R - 1;  // the request owning verify row gi
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (p.rowoff[mid] <= gi) lo = mid; else hi = mid - 1;
+        }
+        req = lo;
+        n = gi - p.rowoff[req];
+        const int len = p.rowoff[req + 1] - p.rowoff[req] - 1;
+        fcol = (n == p.n_acc[req] && n < len) ? req : -1;
+      } else {
+        req = p.rej[r0 + m];
+        n = p.n_acc[req];
+        fcol = r0 + m;
       }
-      row = make_int4(tok, req, n, 0);
+      if (n < p.gamma) {
+        int tok = n == 0 ? p.anchors[req] : p.tokens[static_cast<size_t>(req) * p.gamma + n - 1];
+        if (tok < 0 || tok >= p.V) {
+          report(p.status, DSPARK_STATUS_BAD_TOKEN);
+          tok = 0;
+        }
+        row = make_int4(tok, req, n, fcol);
+      }
     }
     s_rows[m] = row;
+    live = row.x >= 0;
   }
   tc_fence_before_sync();
-  __syncthreads();
+  const int n_live = __syncthreads_count(live);
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t tmem_a = tmem_base + kAccCols;  // A operand columns
@@ -164,10 +192,11 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
         break;
       }
       const uint32_t ubytes = static_cast<uint32_t>(min(kTileN, p.V - v0)) * 4u;
-      if (lane == 0) mbar_arrive_expect_tx(bar_ufull + 8 * s, ubytes * static_cast<uint32_t>(rows_valid));
+      if (lane == 0) mbar_arrive_expect_tx(bar_ufull + 8 * s, ubytes * static_cast<uint32_t>(n_live));
       __syncwarp();
       for (int m = lane; m < rows_valid; m += 32) {
         const int4 row = s_rows[m];
+        if (row.x < 0) continue;
         const size_t urow = static_cast<size_t>(row.y) * p.gamma + row.z;
         bulk_load(base + plan.u[s] + m * kUStride, p.U + urow * p.V + v0, ubytes, bar_ufull + 8 * s, pol_u);
       }
@@ -224,7 +253,8 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
     const int h = (warp - 2) >> 2;  // 32-column half of each tile; half of A's columns
     const int row = q * 32 + lane;
     const int r = r0 + row;
-    const bool valid = row < rows_valid;
+    const bool valid = s_rows[row].x >= 0;
+    const int fcol = s_rows[row].w;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
 
     // A operand: W1[x_row] into tensor memory, K elements [h*rank/2, (h+1)*rank/2)
@@ -265,7 +295,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
       l2zd = p.logZd[static_cast<size_t>(rr.y) * p.gamma + rr.z] * 1.4426950408889634f;
     }
     float runS = 0.f;  // running sum of w over this warp's half of the chunk
-    // a warp with no rejected row in its lane quarter only keeps the rings moving
+    // a warp with no live row in its lane quarter only keeps the rings moving
     const bool warp_works = __any_sync(0xffffffffu, valid);
     for (int i = 0; i < ntile; ++i) {
       const int s = i % kStages, acc = i & 1;
@@ -305,7 +335,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
 
       const int v0 = (t_begin + i) * kTileN + h * kSubN;
       const int ncol = min(kSubN, p.V - v0);  // <= 0 for a fully masked last half
-      const size_t fidx = static_cast<size_t>(2 * (t_begin + i) + h) * p.R_pad + r;
+      const size_t fidx = static_cast<size_t>(2 * (t_begin + i) + h) * p.R_pad + fcol;
       float tv[32];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -320,7 +350,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
         const float pt = exp2f(tv[k] * p.scale - mt) * inv_zt;
         sw += (k < ncol) ? fmaxf(pt - pd, 0.f) : 0.f;
       }
-      if (valid) p.fine[fidx] = make_float2(sw, 0.f);
+      if (valid && fcol >= 0) p.fine[fidx] = make_float2(sw, 0.f);
       runS += sw;
     }
     // combine the two column halves of this CTA's chunk

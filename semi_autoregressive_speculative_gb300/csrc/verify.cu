@@ -16,6 +16,13 @@
 //                   rejected positions fused with max(0, p_t - p_d) partial sums.
 //  k4_residual_sample  one CTA per rejected request: inverse CDF of the
 //                   residual (or of p_t when its mass is zero).
+//
+// Optional output: the analytic acceptance c*_j = 1 - 1/2 ||p_d - p_t||_1
+// ("DSpark" §3.1, eq. c_k*) of every verify row j <= lens[r] that has a draft
+// position (j < gamma).  Then the residual pass covers all those rows instead
+// of the rejected ones only, k4_c_star sums each row's partials, and the
+// rejection sampler reads its rows' partials from the same pass.  Greedy: the
+// two distributions are point masses and k4_accept writes c* = [x_j == argmax].
 #include <cuda.h>
 
 #include <cmath>
@@ -41,6 +48,7 @@ struct VerifyArgs {
   const int32_t* lens;     // [R]
   int32_t* n_accept;       // [R]
   int32_t* next_token;     // [R]
+  float* c_star;           // [R, gamma] or null
   float2* tstats;          // [R*(gamma+1)][n_vc]
   float4* trow;            // [R*(gamma+1)]: (max, Z, t(x), -) base-2 units
   int32_t* rowoff;         // [R+1]
@@ -51,6 +59,7 @@ struct VerifyArgs {
   int R, R_pad, gamma, V, rank, n_vc, n_tiles, n_chunks;
   float scale;             // log2(e) / T (1 when greedy)
   int greedy;
+  int all_rows;            // residual partials cover every verify row with a draft position
   uint64_t seed;
   uint32_t round;
 };
@@ -289,6 +298,13 @@ __global__ void __launch_bounds__(256) k4_accept(const VerifyArgs p) {
       const int nxt = s_am[n];
       p.next_token[r] = (nxt >= 0 && nxt < p.V) ? nxt : 0;
     }
+    if (p.c_star != nullptr) {
+      for (int j = tid; j < p.gamma; j += 256) {
+        const float cs = j <= len ? (p.tokens[static_cast<size_t>(r) * p.gamma + j] == s_am[j] ? 1.f : 0.f)
+                                  : __int_as_float(0x7fc00000);  // NaN: no target row read
+        p.c_star[static_cast<size_t>(r) * p.gamma + j] = cs;
+      }
+    }
     return;
   }
   if (n == len) {
@@ -339,7 +355,11 @@ __global__ void __launch_bounds__(256) k4_residual_sample(const __grid_constant_
   const float Mt = ts.x;
   const float Zt = ts.y;
   const float u2 = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(n), kResidualOrBonus);
-  const float2* crow = p.coarse + static_cast<size_t>(i) * p.n_chunks;
+  // partials of this row: by rejection slot, or (all verify rows covered) by
+  // verify row for the chunk sums and by request for the sub-tile sums
+  const int prow = p.all_rows ? p.rowoff[r] + n : i;
+  const int fcol = p.all_rows ? r : i;
+  const float2* crow = p.coarse + static_cast<size_t>(prow) * p.n_chunks;
   float zl = 0.f;
   for (int c = tid; c < p.n_chunks; c += 256) zl += crow[c].x;
   const float Zr = block_sum_f(zl, s_redz);
@@ -355,7 +375,7 @@ __global__ void __launch_bounds__(256) k4_residual_sample(const __grid_constant_
       p.n_chunks, 0.f, target, [&](int c) -> float { return crow[c].x; }, &before_c, sc);
   const int tb = static_cast<int>((static_cast<long long>(cstar) * p.n_tiles) / p.n_chunks);
   const int te = static_cast<int>((static_cast<long long>(cstar + 1) * p.n_tiles) / p.n_chunks);
-  const float2* frow = p.fine + i;
+  const float2* frow = p.fine + fcol;
   float before_s = 0.f;
   const int sstar = 2 * tb + block_find_crossing<256>(
                                  2 * (te - tb), before_c, target,
@@ -410,6 +430,27 @@ __global__ void __launch_bounds__(256) k4_residual_sample(const __grid_constant_
   }
 }
 
+// c*_{r,j} = 1 - sum over the vocabulary of max(0, p_t - p_d), from the chunk
+// partials of verify row rowoff[r] + j; one warp per (r, j), a fixed summation
+// order; NaN for positions past the rows verify read.
+__global__ void __launch_bounds__(256) k4_c_star(const VerifyArgs p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (gw >= p.R * p.gamma) return;
+  const int r = gw / p.gamma, j = gw - r * p.gamma;
+  const int len = clamp_len(p.lens[r], p.gamma, nullptr);
+  float cs = __int_as_float(0x7fc00000);
+  if (j <= len) {
+    const float2* crow = p.coarse + static_cast<size_t>(p.rowoff[r] + j) * p.n_chunks;
+    float s = 0.f;
+    for (int c = lane; c < p.n_chunks; c += 32) s += crow[c].x;
+    cs = 1.f - warp_sum(s);
+  }
+  if (lane == 0) p.c_star[gw] = cs;
+}
+
 // The residual pass of verify, chained to the accept kernel with programmatic
 // dependent launch.
 static cudaError_t launch_residual_partials(const CUtensorMap& tm_w2, const ResidualArgs& a, cudaStream_t stream) {
@@ -426,12 +467,12 @@ static cudaError_t launch_residual_partials(const CUtensorMap& tm_w2, const Resi
 int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors,
                   const int32_t* tokens, const float* pd_tok, const float* logZ, const int32_t* lens, int R, int gamma,
                   int V, int rank, float temperature, uint64_t seed, uint32_t round, int32_t* n_accept,
-                  int32_t* next_token, void* workspace, cudaStream_t stream) {
+                  int32_t* next_token, float* c_star, void* workspace, cudaStream_t stream) {
   const WorkspaceLayout L = workspace_layout(R, gamma, V);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   VerifyArgs p = {};
   p.T = T; p.U = U; p.W1 = W1; p.W2 = W2; p.anchors = anchors; p.tokens = tokens; p.pd_tok = pd_tok;
-  p.logZd = logZ; p.lens = lens; p.n_accept = n_accept; p.next_token = next_token;
+  p.logZd = logZ; p.lens = lens; p.n_accept = n_accept; p.next_token = next_token; p.c_star = c_star;
   p.tstats = reinterpret_cast<float2*>(ws + L.tstats);
   p.trow = reinterpret_cast<float4*>(ws + L.trow);
   p.rowoff = reinterpret_cast<int32_t*>(ws + L.rowoff);
@@ -444,8 +485,14 @@ int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint
   p.R_pad = n_mtiles * kMTile;
   p.n_vc = ceil_div(V, kVerifyChunk);
   p.n_tiles = ceil_div(V, kTileN);
-  p.n_chunks = vocab_chunks(p.n_tiles, n_mtiles);
   p.greedy = temperature == 0.0f ? 1 : 0;
+  // residual rows: the rejected requests (<= R), or every verify row (<= R (gamma + 1))
+  p.all_rows = (c_star != nullptr && !p.greedy) ? 1 : 0;
+  const int res_mtiles = p.all_rows ? ceil_div(R * (gamma + 1), kMTile) : n_mtiles;
+  p.n_chunks = vocab_chunks(p.n_tiles, res_mtiles);
+  // the chunk partials of every residual row must fit the workspace's partials region
+  if (static_cast<size_t>(res_mtiles) * kMTile * p.n_chunks > static_cast<size_t>(kMaxChunks) * p.R_pad)
+    return DSPARK_ERR_UNSUPPORTED_SHAPE;
   p.scale = p.greedy ? 1.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   p.seed = seed; p.round = round;
 
@@ -470,15 +517,19 @@ int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint
   ResidualArgs a = {};
   a.U = U; a.W1 = W1; a.W2 = W2; a.anchors = anchors; a.tokens = tokens;
   a.T = T; a.rej = p.rej; a.n_acc = n_accept; a.trow = p.trow; a.logZd = logZ;
+  a.rowoff = p.all_rows ? p.rowoff : nullptr;
   a.coarse = reinterpret_cast<float2*>(ws + L.coarse);
   a.fine = reinterpret_cast<float2*>(ws + L.fine);
   a.status = p.status;
   a.R = R; a.R_pad = p.R_pad; a.gamma = gamma; a.V = V; a.rank = rank;
-  a.n_tiles = p.n_tiles; a.n_chunks = p.n_chunks; a.n_mtiles = n_mtiles;
+  a.n_tiles = p.n_tiles; a.n_chunks = p.n_chunks; a.n_mtiles = res_mtiles;
   a.scale = p.scale;
   CUtensorMap tm_w2;
   if (encode_w2_map(&tm_w2, W2, V, rank) != DSPARK_OK) return DSPARK_ERR_CUDA;
   if (launch_residual_partials(tm_w2, a, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (p.all_rows &&
+      launch_pdl(k4_c_star, dim3(ceil_div(R * gamma, 8)), dim3(256), 0, stream, true, p) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   CUtensorMap tm_slab;
   if (encode_w2_slab_map(&tm_slab, W2, V, rank) != DSPARK_OK) return DSPARK_ERR_CUDA;
   if (launch_pdl(k4_residual_sample, dim3(R), dim3(256), 0, stream, true, tm_slab, p) != cudaSuccess)

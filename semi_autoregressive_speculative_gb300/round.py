@@ -47,6 +47,7 @@ class DeviceRound:
         self.theta = torch.zeros((1,), dtype=torch.float64, device=dv)
         self.n_accept = torch.empty((R,), dtype=i32, device=dv)
         self.next_token = torch.empty((R,), dtype=i32, device=dv)
+        self.c_star = torch.empty((R, gamma), dtype=f32, device=dv)
         ws = dspark_workspace_size(R, gamma, V, rank, d)
         if ws == 0:
             raise ValueError("invalid sizes")
@@ -78,11 +79,13 @@ class DeviceRound:
         dspark_schedule(self.a if a is None else a, self.sps, mode, budget_K, self.lens, self.sched_out[0:1],
                         self.sched_out[1:2], self.theta, self.workspace)
 
-    def verify(self, temperature: float, seed: int, rnd: int, tokens=None, pd=None, logZ=None, lens=None):
+    def verify(self, temperature: float, seed: int, rnd: int, tokens=None, pd=None, logZ=None, lens=None,
+               c_star: bool = False):
+        """c_star=True also writes the analytic acceptance into self.c_star."""
         dspark_verify(self.T, self.U, self.W1, self.W2, self.anchors, self.tokens if tokens is None else tokens,
                       self.pd if pd is None else pd, self.logZ if logZ is None else logZ,
                       self.lens if lens is None else lens, temperature, seed, rnd, self.n_accept,
-                      self.next_token, self.workspace)
+                      self.next_token, self.workspace, c_star=self.c_star if c_star else None)
 
     def clear_status(self):
         dspark_clear_status(self.workspace)

@@ -85,7 +85,7 @@ def test_confidence_and_verify_validation(L):
 
     def verify(T=FAKE, V=4096, temp=1.0, wsb=1 << 30):
         return L.dspark_verify(T, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 7, V, 256, temp, 0, 0,
-                               FAKE, FAKE, FAKE, wsb, None)
+                               FAKE, FAKE, None, FAKE, wsb, None)
     assert verify(T=0) == -1
     assert verify(T=FAKE + 4) == -1
     assert verify(V=12) == -2

@@ -56,3 +56,66 @@ def test_verify_full_size_sampled(name):
     for temperature in wl.temperatures:
         na, nx, ex = _run(wl, temperature, sample_requests(wl.R))
         assert ex <= 1
+
+
+def _run_c_star(wl, temperature, compare, lens=None, rnd=0):
+    """Verify twice, without and with the analytic acceptance c*; the two
+    calls must agree on every emitted token, and c* must match the oracle."""
+    import oracle
+    from gpu_helpers import PROB_TOL, weights
+    dr, inp = device_round(wl)
+    tokens, pd, lz, T, lens = verify_inputs(wl, inp, rnd, compare, temperature, lens)
+    dr.T.copy_(torch.from_numpy(T))
+    dr.tokens.copy_(torch.from_numpy(tokens))
+    dr.pd.copy_(torch.from_numpy(pd))
+    dr.logZ.copy_(torch.from_numpy(lz))
+    dr.lens.copy_(torch.from_numpy(lens))
+    dr.verify(temperature, wl.seed, rnd)
+    na0, nx0 = host(dr.n_accept), host(dr.next_token)
+    dr.c_star.fill_(-5.0)
+    dr.verify(temperature, wl.seed, rnd, c_star=True)
+    na, nx, cs = host(dr.n_accept), host(dr.next_token), host(dr.c_star)
+    assert np.array_equal(na, na0) and np.array_equal(nx, nx0)
+    assert dr.status() == 0
+    # rows past lens[r] were not read: NaN there, a value everywhere else
+    j = np.arange(wl.gamma)[None, :]
+    assert np.array_equal(np.isnan(cs), j > lens[:, None])
+    W1, W2, _ = weights(wl)
+    cmp_ = np.asarray(compare)
+    cs_o = oracle.c_star(T[cmp_], inp.U[cmp_], W1, W2, inp.anchors[cmp_], tokens[cmp_], lens[cmp_], temperature)
+    got = cs[cmp_]
+    assert np.array_equal(np.isnan(got), np.isnan(cs_o))
+    m = ~np.isnan(cs_o)
+    if temperature == 0.0:
+        assert np.array_equal(got[m], cs_o[m])
+    else:
+        assert np.max(np.abs(got[m] - cs_o[m])) <= PROB_TOL
+    ex = check_verify(wl, inp, T, tokens, lens, na, nx, temperature, rnd, compare)
+    return cs, ex
+
+
+@pytest.mark.parametrize("temperature", [1.0, 0.7, 0.0])
+def test_c_star_tiny(temperature):
+    _, ex = _run_c_star(TINY, temperature, range(TINY.R))
+    assert ex <= 1
+
+
+@pytest.mark.parametrize("temperature", [1.0, 0.0])
+def test_c_star_ragged_lengths(temperature):
+    wl = synth.scaled(TINY, R=9, gamma=5, V=1000, d=16, name="ragged_verify")
+    lens = np.array([0, 1, 2, 3, 4, 5, 5, 0, 2], np.int32)
+    _, ex = _run_c_star(wl, temperature, range(wl.R), lens=lens)
+    assert ex <= 1
+
+
+def test_c_star_many_mtiles():
+    # 140 requests x up to 4 verify rows: residual rows over five M-tiles
+    wl = synth.scaled(TINY, R=140, gamma=3, V=2048, rank=128, d=16, name="verify_r140")
+    _, ex = _run_c_star(wl, 1.0, range(0, 140, 7))
+    assert ex <= 1
+
+
+def test_c_star_full_size():
+    wl = synth.WORKLOADS["r128_g16_v151936"]
+    _, ex = _run_c_star(wl, 1.0, sample_requests(wl.R))
+    assert ex <= 1
