@@ -39,18 +39,30 @@ DEFAULT_WORKLOAD = "r128_g16_v151936"
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes per dspark_markov_draft call (one round's 16 positions) from the
-# ncu capture summarised in profiles/; valid only for the kernel sources
-# whose digest is recorded with it.
-NCU_DRAFT_TRAFFIC = {"digest": "fb28b86db73f", "bytes_per_call": 1.93e9 + 51.91e6}
+# ncu capture summarised in profiles/; valid only for the draft kernel sources
+# whose digest (draft_digest) is recorded with it.
+NCU_DRAFT_TRAFFIC = {"digest": "997f83ac25e4", "bytes_per_call": 1.93e9 + 52.56e6}
 
 
 # ----------------------------------------------------------------------------- helpers
-def kernel_digest() -> str:
+def _digest(paths) -> str:
     h = hashlib.sha1()
-    for f in sorted(glob.glob(os.path.join(ROOT, "semi_autoregressive_speculative_gb300", "csrc", "*"))):
+    for f in sorted(paths):
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
+
+
+def kernel_digest() -> str:
+    """Digest of every kernel source of the library."""
+    return _digest(glob.glob(os.path.join(ROOT, "semi_autoregressive_speculative_gb300", "csrc", "*")))
+
+
+def draft_digest() -> str:
+    """Digest of the sources the draft kernel is compiled from."""
+    csrc = os.path.join(ROOT, "semi_autoregressive_speculative_gb300", "csrc")
+    names = ["markov_draft.cu", "common.h", "device.cuh", "search.cuh", "vocab_common.h"]
+    return _digest([os.path.join(csrc, n) for n in names] + [os.path.join(ROOT, "include", "dspark.h")])
 
 
 def measured_peaks():
@@ -360,7 +372,7 @@ def run_gpu(args):
     cstar_rows = int(np.minimum(lens_h + 1, g).sum()) if temp > 0 else 0
     cstar_bytes = rows_read * V * 4 + cstar_rows * V * 8 + (rk * V * 2 if cstar_rows else 0)
     digest = kernel_digest()
-    traffic = NCU_DRAFT_TRAFFIC["bytes_per_call"] if NCU_DRAFT_TRAFFIC["digest"] == digest else None
+    traffic = NCU_DRAFT_TRAFFIC["bytes_per_call"] if NCU_DRAFT_TRAFFIC["digest"] == draft_digest() else None
 
     # ------------------------------------------------------------- end to end (host buffers)
     e2e = None

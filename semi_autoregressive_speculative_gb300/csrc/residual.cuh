@@ -14,7 +14,11 @@
 // Summed over the vocabulary, w gives 1 - c* for that row ("DSpark" §3.1,
 // eq. c_k*: sum max(0, p_t - p_d) = 1/2 ||p_d - p_t||_1).
 //
-// One CTA per (contiguous V-chunk, M-tile), 10 warps:
+// One CTA per (contiguous V-chunk, M-tile), 10 warps.  The number of rows is
+// decided on the device (rejections, or the verify lengths), so the launch
+// has at least one CTA per SM and the split of the vocabulary into chunks is
+// taken on the device from the actual row count (residual_chunks); the
+// kernels that read the partials take the same split.
 //   warp 0     producer: W2 tiles by TMA (MN-major, 128B-swizzled) into a
 //              kStages-deep ring freed by the UMMA, and the gathered U rows by
 //              per-row bulk copies into a second ring freed by the epilogue;
@@ -47,14 +51,26 @@ struct ResidualArgs {
   const int32_t* rowoff;   // [R+1] verify row offsets; non-null: one row per verify row with a draft position
   const float4* trow;      // [R*(gamma+1)] (max, Z) of each target row, base-2 units
   const float* logZd;      // [R, gamma] draft log-normaliser (natural log)
-  float2* coarse;          // [row][n_chunks]: x = sum of w over the chunk
+  float2* coarse;          // [row][residual_chunks(rows)]: x = sum of w over the chunk
   float2* fine;            // [2 * n_tiles][R_pad]: x = sum of w over the 32-column sub-tile, rejected
                            // rows only (column = rejection slot, or request when rowoff is set)
   int32_t* status;
   int R, R_pad, gamma, V, rank;
-  int n_tiles, n_chunks, n_mtiles;
+  int n_tiles;
+  int grid;                // CTAs launched
   float scale;             // log2(e) / T
 };
+
+// Vocabulary chunks per M-tile for `rows` residual rows and `grid` CTAs: as
+// many as keep every CTA busy, at most one 64-column tile each.
+__host__ __device__ inline int residual_chunks(int rows, int grid, int n_tiles) {
+  const int mt = rows > 0 ? (rows + kMTile - 1) / kMTile : 1;
+  int c = grid / mt;
+  if (c < 1) c = 1;
+  if (c > n_tiles) c = n_tiles;
+  if (c > kMaxChunks) c = kMaxChunks;
+  return c;
+}
 
 struct ResidualSmem {
   uint32_t w[kStages], u[kStages], half, bars, rows, total;
@@ -80,16 +96,17 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
   const ResidualSmem plan = residual_smem_plan(p.rank);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mtile = blockIdx.x % p.n_mtiles;
-  const int chunk = blockIdx.x / p.n_mtiles;
-  const int r0 = mtile * kMTile;
-
   pdl_wait();
   const int nrows = p.rowoff != nullptr ? p.rowoff[p.R] : p.rej[p.R_pad];
-  if (r0 >= nrows) return;  // no residual rows for this M-tile
+  const int n_mt = (nrows + kMTile - 1) / kMTile;
+  const int n_chunks = residual_chunks(nrows, p.grid, p.n_tiles);
+  if (static_cast<int>(blockIdx.x) >= n_mt * n_chunks) return;  // no work for this CTA
+  const int mtile = blockIdx.x % n_mt;
+  const int chunk = blockIdx.x / n_mt;
+  const int r0 = mtile * kMTile;
   const int rows_valid = min(kMTile, nrows - r0);
-  const int t_begin = static_cast<int>((static_cast<long long>(chunk) * p.n_tiles) / p.n_chunks);
-  const int t_end = static_cast<int>((static_cast<long long>(chunk + 1) * p.n_tiles) / p.n_chunks);
+  const int t_begin = static_cast<int>((static_cast<long long>(chunk) * p.n_tiles) / n_chunks);
+  const int t_end = static_cast<int>((static_cast<long long>(chunk + 1) * p.n_tiles) / n_chunks);
   const int ntile = t_end - t_begin;
 
   const uint32_t bar_wfull = base + plan.bars;         // [kStages]
@@ -356,7 +373,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
     // combine the two column halves of this CTA's chunk
     if (h == 1) s_half[row] = make_float2(0.f, runS);
     named_barrier(1, 256);
-    if (h == 0 && valid) p.coarse[static_cast<size_t>(r) * p.n_chunks + chunk] = make_float2(runS + s_half[row].y, 0.f);
+    if (h == 0 && valid) p.coarse[static_cast<size_t>(r) * n_chunks + chunk] = make_float2(runS + s_half[row].y, 0.f);
   }
   if (*abort_flag && threadIdx.x == 0) report(p.status, DSPARK_STATUS_TIMEOUT);
   tc_fence_before_sync();

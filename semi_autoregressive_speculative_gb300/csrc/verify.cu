@@ -25,6 +25,7 @@
 // two distributions are point masses and k4_accept writes c* = [x_j == argmax].
 #include <cuda.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -53,10 +54,11 @@ struct VerifyArgs {
   float4* trow;            // [R*(gamma+1)]: (max, Z, t(x), -) base-2 units
   int32_t* rowoff;         // [R+1]
   int32_t* rej;            // [R_pad + 1]
-  const float2* coarse;    // residual partials [R_pad][n_chunks]
+  const float2* coarse;    // residual partials [row][residual_chunks(rows, res_grid, n_tiles)]
   const float2* fine;      // [2*n_tiles][R_pad]
   int32_t* status;
-  int R, R_pad, gamma, V, rank, n_vc, n_tiles, n_chunks;
+  int R, R_pad, gamma, V, rank, n_vc, n_tiles;
+  int res_grid;            // CTAs of the residual pass
   float scale;             // log2(e) / T (1 when greedy)
   int greedy;
   int all_rows;            // residual partials cover every verify row with a draft position
@@ -359,9 +361,10 @@ __global__ void __launch_bounds__(256) k4_residual_sample(const __grid_constant_
   // verify row for the chunk sums and by request for the sub-tile sums
   const int prow = p.all_rows ? p.rowoff[r] + n : i;
   const int fcol = p.all_rows ? r : i;
-  const float2* crow = p.coarse + static_cast<size_t>(prow) * p.n_chunks;
+  const int n_chunks = residual_chunks(p.all_rows ? p.rowoff[p.R] : p.rej[p.R_pad], p.res_grid, p.n_tiles);
+  const float2* crow = p.coarse + static_cast<size_t>(prow) * n_chunks;
   float zl = 0.f;
-  for (int c = tid; c < p.n_chunks; c += 256) zl += crow[c].x;
+  for (int c = tid; c < n_chunks; c += 256) zl += crow[c].x;
   const float Zr = block_sum_f(zl, s_redz);
   if (!(Zr > 0.f) || !(Zr <= 3.4e38f)) {
     // zero residual mass: draw from p_t
@@ -372,9 +375,9 @@ __global__ void __launch_bounds__(256) k4_residual_sample(const __grid_constant_
   const float target = u2 * Zr;
   float before_c = 0.f;
   const int cstar = block_find_crossing<256>(
-      p.n_chunks, 0.f, target, [&](int c) -> float { return crow[c].x; }, &before_c, sc);
-  const int tb = static_cast<int>((static_cast<long long>(cstar) * p.n_tiles) / p.n_chunks);
-  const int te = static_cast<int>((static_cast<long long>(cstar + 1) * p.n_tiles) / p.n_chunks);
+      n_chunks, 0.f, target, [&](int c) -> float { return crow[c].x; }, &before_c, sc);
+  const int tb = static_cast<int>((static_cast<long long>(cstar) * p.n_tiles) / n_chunks);
+  const int te = static_cast<int>((static_cast<long long>(cstar + 1) * p.n_tiles) / n_chunks);
   const float2* frow = p.fine + fcol;
   float before_s = 0.f;
   const int sstar = 2 * tb + block_find_crossing<256>(
@@ -443,9 +446,10 @@ __global__ void __launch_bounds__(256) k4_c_star(const VerifyArgs p) {
   const int len = clamp_len(p.lens[r], p.gamma, nullptr);
   float cs = __int_as_float(0x7fc00000);
   if (j <= len) {
-    const float2* crow = p.coarse + static_cast<size_t>(p.rowoff[r] + j) * p.n_chunks;
+    const int n_chunks = residual_chunks(p.rowoff[p.R], p.res_grid, p.n_tiles);
+    const float2* crow = p.coarse + static_cast<size_t>(p.rowoff[r] + j) * n_chunks;
     float s = 0.f;
-    for (int c = lane; c < p.n_chunks; c += 32) s += crow[c].x;
+    for (int c = lane; c < n_chunks; c += 32) s += crow[c].x;
     cs = 1.f - warp_sum(s);
   }
   if (lane == 0) p.c_star[gw] = cs;
@@ -455,7 +459,7 @@ __global__ void __launch_bounds__(256) k4_c_star(const VerifyArgs p) {
 // dependent launch.
 static cudaError_t launch_residual_partials(const CUtensorMap& tm_w2, const ResidualArgs& a, cudaStream_t stream) {
   const ResidualSmem plan = residual_smem_plan(a.rank);
-  const dim3 grid(a.n_chunks * a.n_mtiles);
+  const dim3 grid(a.grid);
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(k_residual_partials, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -488,10 +492,12 @@ int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint
   p.greedy = temperature == 0.0f ? 1 : 0;
   // residual rows: the rejected requests (<= R), or every verify row (<= R (gamma + 1))
   p.all_rows = (c_star != nullptr && !p.greedy) ? 1 : 0;
+  // one CTA per SM at least, one per M-tile of the most rows there can be
   const int res_mtiles = p.all_rows ? ceil_div(R * (gamma + 1), kMTile) : n_mtiles;
-  p.n_chunks = vocab_chunks(p.n_tiles, res_mtiles);
-  // the chunk partials of every residual row must fit the workspace's partials region
-  if (static_cast<size_t>(res_mtiles) * kMTile * p.n_chunks > static_cast<size_t>(kMaxChunks) * p.R_pad)
+  p.res_grid = std::max(sm_count(), res_mtiles);
+  // the chunk partials of every residual row (at most 128 x max(grid, M-tiles)
+  // entries) must fit the workspace's partials region
+  if (static_cast<size_t>(p.res_grid) * kMTile > static_cast<size_t>(kMaxChunks) * p.R_pad)
     return DSPARK_ERR_UNSUPPORTED_SHAPE;
   p.scale = p.greedy ? 1.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   p.seed = seed; p.round = round;
@@ -522,7 +528,7 @@ int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint
   a.fine = reinterpret_cast<float2*>(ws + L.fine);
   a.status = p.status;
   a.R = R; a.R_pad = p.R_pad; a.gamma = gamma; a.V = V; a.rank = rank;
-  a.n_tiles = p.n_tiles; a.n_chunks = p.n_chunks; a.n_mtiles = res_mtiles;
+  a.n_tiles = p.n_tiles; a.grid = p.res_grid;
   a.scale = p.scale;
   CUtensorMap tm_w2;
   if (encode_w2_map(&tm_w2, W2, V, rank) != DSPARK_OK) return DSPARK_ERR_CUDA;
