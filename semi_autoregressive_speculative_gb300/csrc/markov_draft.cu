@@ -73,14 +73,19 @@ struct DraftArgs {
   uint32_t round;
 };
 
+// Offsets in dynamic shared memory.  Ring stages are found by arithmetic
+// (w0 + s * wstride), never by indexing an array with the stage number: a
+// runtime-indexed array would put the whole plan in local memory.
 struct DraftSmem {
-  uint32_t w[kDraftWStages], u[kDraftUStages], half, bars, slots, part, wts, ev, slab, total;
+  uint32_t w0, wstride, u0, half, bars, slots, part, wts, ev, slab, total;
+  __host__ __device__ uint32_t w(int s) const { return w0 + static_cast<uint32_t>(s) * wstride; }
+  __host__ __device__ uint32_t u(int s) const { return u0 + static_cast<uint32_t>(s) * kDraftUBytes; }
 };
 __host__ __device__ inline DraftSmem draft_smem_plan(int rank) {
   DraftSmem s;
   uint32_t off = 0;
-  for (int i = 0; i < kDraftWStages; ++i) { s.w[i] = off; off += 128u * rank; }  // rank x 64 bf16, SW128
-  for (int i = 0; i < kDraftUStages; ++i) { s.u[i] = off; off += kDraftUBytes; }
+  s.w0 = off; s.wstride = 128u * rank; off += kDraftWStages * s.wstride;  // rank x 64 bf16, SW128
+  s.u0 = off; off += kDraftUStages * kDraftUBytes;
   s.half = off; off += kMTile * 8;
   s.bars = off; off += 256;
   s.slots = off; off += 32;                      // the sampler's SampleSlot
@@ -309,11 +314,13 @@ struct SampleSmem {
 // shared memory), and copies that sub-tile's W2 columns (one TMA box,
 // rank x 32) and U values (one bulk copy) into shared memory.  Each warp then
 // sums its 32 rank rows for the 32 columns (a lane per column), and the leader
-// adds the shares and U and picks the token.  Returns false (the same in every
-// warp: it follows the slot, read after a barrier) when the leader's wait gave
-// up.
-__device__ __forceinline__ bool sample_cta(const DraftArgs& p, const CUtensorMap* tm_slab, int r, int step, int sub,
-                                        const SampleSmem& sm, uint32_t& phase, volatile int* abort_flag) {
+// adds the shares and U and picks the token.  Returns the number of slab copies
+// waited for (0 or 1: add it to `phase`), or -1 (the same in every warp: it
+// follows the slot, read after a barrier) when the leader's wait gave up.  The
+// arguments are plain values so that nothing of the sampler lives in local
+// memory.
+__device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap* tm_slab, int r, int step, int sub,
+                                       const SampleSmem sm, const uint32_t phase, volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
   const size_t out = static_cast<size_t>(r) * p.gamma + step;
   SampleSlot& slot = *sm.slot;
@@ -407,7 +414,6 @@ __device__ __forceinline__ bool sample_cta(const DraftArgs& p, const CUtensorMap
   if (state == kSlotSample) {
     landed = __all_sync(0xffffffffu, mbar_wait(sm.bar, phase & 1u, abort_flag));
     if (!landed) *abort_flag = 1;
-    ++phase;
     // this warp's share of the 32 bias values: lane l sums column v0 + l over
     // the warp's rank rows (W1 entries read as shared-memory broadcasts)
     float acc = 0.f;
@@ -469,7 +475,7 @@ __device__ __forceinline__ bool sample_cta(const DraftArgs& p, const CUtensorMap
   // the slot, the shares and the slab are rewritten for the next request only
   // after that request's first barrier, which the leader reaches only after
   // it has finished reading them here
-  return state != kSlotAbort;
+  return state == kSlotAbort ? -1 : (state == kSlotSample ? 1 : 0);
 }
 
 template <bool kGreedy>
@@ -551,7 +557,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(bar_wfull + 8 * sw, wbytes);
-        tma_load_2d(base + plan.w[sw], &tm_w2, bar_wfull + 8 * sw, v0, 0, pol_w);
+        tma_load_2d(base + plan.w(sw), &tm_w2, bar_wfull + 8 * sw, v0, 0, pol_w);
         ++wfilled;
         if (!mbar_wait(bar_uempty + 8 * su, ((it / kDraftUStages) & 1) ^ 1, abort_flag)) {
           *abort_flag = 1;
@@ -559,7 +565,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
         }
         // one 128-row x 68-column box; rows past R and columns past V are zero-filled
         mbar_arrive_expect_tx(bar_ufull + 8 * su, kDraftUBytes);
-        tma_load_3d(base + plan.u[su], &tm_u, bar_ufull + 8 * su, v0, step, r0, pol_u);
+        tma_load_3d(base + plan.u(su), &tm_u, bar_ufull + 8 * su, v0, step, r0, pol_u);
         ++ufilled;
       }
       if (*abort_flag) {
@@ -596,7 +602,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
           tc_fence_after_sync();
           const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
           for (int ks = 0; ks < ksteps; ++ks) {
-            const uint32_t b_addr = base + plan.w[sw] + ks * 2048;
+            const uint32_t b_addr = base + plan.w(sw) + ks * 2048;
             umma_bf16_ts(d, tmem_a + ks * 8, smem_desc_sw128(b_addr, 1024, 1024), idesc, ks > 0 ? 1u : 0u);
           }
           umma_commit(bar_wempty + 8 * sw);
@@ -697,7 +703,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
             break;
           }
           const float4* urow =
-              reinterpret_cast<const float4*>(gbase + plan.u[su] + row * (kDraftUCols * 4) + h * (kSubN * 4));
+              reinterpret_cast<const float4*>(gbase + plan.u(su) + row * (kDraftUCols * 4) + h * (kSubN * 4));
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const float4 t4 = urow[k];
@@ -787,10 +793,12 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
       } else {
         // all 8 epilogue warps on each of this CTA's requests in turn
         for (int rr = blockIdx.x; rr < p.R; rr += gridDim.x) {
-          if (!sample_cta(p, &tm_slab, rr, step, warp - 2, ssm, slab_phase, abort_flag)) {
+          const int rc = sample_cta(p, &tm_slab, rr, step, warp - 2, ssm, slab_phase, abort_flag);
+          if (rc < 0) {
             *abort_flag = 1;
             break;
           }
+          slab_phase += static_cast<uint32_t>(rc);
         }
       }
     }

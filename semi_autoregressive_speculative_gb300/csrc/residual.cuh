@@ -72,14 +72,18 @@ __host__ __device__ inline int residual_chunks(int rows, int grid, int n_tiles) 
   return c;
 }
 
+// Ring stages by arithmetic (w0 + s * wstride): a runtime-indexed array of
+// offsets would live in local memory.
 struct ResidualSmem {
-  uint32_t w[kStages], u[kStages], half, bars, rows, total;
+  uint32_t w0, wstride, u0, half, bars, rows, total;
+  __host__ __device__ uint32_t w(int s) const { return w0 + static_cast<uint32_t>(s) * wstride; }
+  __host__ __device__ uint32_t u(int s) const { return u0 + static_cast<uint32_t>(s) * (kMTile * kUStride); }
 };
 __host__ __device__ inline ResidualSmem residual_smem_plan(int rank) {
   ResidualSmem s;
   uint32_t off = 0;
-  for (int i = 0; i < kStages; ++i) { s.w[i] = off; off += 128u * rank; }       // rank x 64 bf16, MN-major SW128
-  for (int i = 0; i < kStages; ++i) { s.u[i] = off; off += kMTile * kUStride; } // 128 rows x 64 fp32, padded rows
+  s.w0 = off; s.wstride = 128u * rank; off += kStages * s.wstride;  // rank x 64 bf16, MN-major SW128
+  s.u0 = off; off += kStages * kMTile * kUStride;                     // 128 rows x 64 fp32, padded rows
   s.half = off; off += kMTile * 8;   // second-half chunk partials
   s.bars = off; off += 256;          // mbarriers, tmem slot, abort flag
   s.rows = off; off += kMTile * 16;  // residual rows: token, request, position, fine column
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
       }
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_wfull + 8 * s, wbytes);
-        tma_load_2d(base + plan.w[s], &tm_w2, bar_wfull + 8 * s, v0, 0, pol_w);
+        tma_load_2d(base + plan.w(s), &tm_w2, bar_wfull + 8 * s, v0, 0, pol_w);
       }
       ok = lane == 0 ? mbar_wait(bar_uempty + 8 * s, ph ^ 1, abort_flag) : true;
       if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -215,7 +219,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
         const int4 row = s_rows[m];
         if (row.x < 0) continue;
         const size_t urow = static_cast<size_t>(row.y) * p.gamma + row.z;
-        bulk_load(base + plan.u[s] + m * kUStride, p.U + urow * p.V + v0, ubytes, bar_ufull + 8 * s, pol_u);
+        bulk_load(base + plan.u(s) + m * kUStride, p.U + urow * p.V + v0, ubytes, bar_ufull + 8 * s, pol_u);
       }
       __syncwarp();
       ++filled;
@@ -249,7 +253,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
         tc_fence_after_sync();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
         for (int ks = 0; ks < ksteps; ++ks) {
-          const uint32_t b_addr = base + plan.w[s] + ks * 2048;
+          const uint32_t b_addr = base + plan.w(s) + ks * 2048;
           umma_bf16_ts(d, tmem_a + ks * 8, smem_desc_sw128(b_addr, 1024, 1024), idesc, ks > 0 ? 1u : 0u);
         }
         umma_commit(bar_wempty + 8 * s);
@@ -341,7 +345,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
         break;
       }
       float u[32];
-      const float4* urow = reinterpret_cast<const float4*>(gbase + plan.u[s] + row * kUStride + h * 128);
+      const float4* urow = reinterpret_cast<const float4*>(gbase + plan.u(s) + row * kUStride + h * 128);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const float4 t4 = urow[k];
