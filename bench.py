@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per dspark_markov_draft call (one round's 16 positions) from the
 # ncu capture summarised in profiles/; valid only for the draft kernel sources
 # whose digest (draft_digest) is recorded with it.
-NCU_DRAFT_TRAFFIC = {"digest": "997f83ac25e4", "bytes_per_call": 1.93e9 + 52.56e6}
+NCU_DRAFT_TRAFFIC = {"digest": "a4ec736d5a8a", "bytes_per_call": 1.91e9 + 50.23e6}
 
 
 # ----------------------------------------------------------------------------- helpers

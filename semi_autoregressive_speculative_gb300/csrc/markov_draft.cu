@@ -253,7 +253,9 @@ __device__ __forceinline__ void publish_token(const DraftArgs& p, int r, int ste
 }
 
 // Greedy sampler for request r (one warp, every chunk partial of its M-tile
-// visible): the argmax of the chunk partials, lowest index on ties.
+// visible): the argmax of the chunk partials, lowest index on ties.  Partials
+// and tokens that other CTAs write during the call are read through L2
+// (ld.global.cg): this SM's L1 may hold the previous position's lines.
 __device__ __forceinline__ void sample_greedy(const DraftArgs& p, int r, int step) {
   const int lane = threadIdx.x & 31;
   const size_t out = static_cast<size_t>(r) * p.gamma + step;
@@ -263,7 +265,7 @@ __device__ __forceinline__ void sample_greedy(const DraftArgs& p, int r, int ste
 #pragma unroll
   for (int k = 0; k < kMaxSampleChunks / 32; ++k) {
     const int c = k * 32 + lane;
-    const float2 e = c < p.n_chunks ? crow[c] : make_float2(-INFINITY, 0.f);
+    const float2 e = c < p.n_chunks ? __ldcg(crow + c) : make_float2(-INFINITY, 0.f);
     const int ei = __float_as_int(e.y);
     if (e.x > best || (e.x == best && e.x > -INFINITY && ei < bidx)) { best = e.x; bidx = ei; }
   }
@@ -326,7 +328,7 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
   SampleSlot& slot = *sm.slot;
 
   // issued before the wait: the previous token's W1 entry of this lane's rank row
-  const int prev_raw = step == 0 ? p.anchors[r] : p.tokens[out - 1];
+  const int prev_raw = step == 0 ? p.anchors[r] : __ldcg(p.tokens + out - 1);
   const int prev = (prev_raw >= 0 && prev_raw < p.V) ? prev_raw : 0;
   const int j = sub * 32 + lane;  // this lane's rank row (rank <= 256: one row per lane)
   sm.ev[j] = j < p.rank ? bf16_at(p.W1 + static_cast<size_t>(prev) * p.rank + j) : 0.f;
@@ -337,6 +339,7 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
     if (lane == 0)
       ok = wait_at_least(p.done + 16 * (r / kMTile), static_cast<uint32_t>(p.n_chunks * (step + 1)), p.abort);
     ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();  // the other lanes' loads below are ordered after lane 0's acquire
     int state = kSlotAbort, sstar = 0;
     float M = 0.f, Z = 0.f, target = 0.f, before_s = 0.f;
     if (ok) {
@@ -346,7 +349,7 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
 #pragma unroll
       for (int k = 0; k < KC; ++k) {
         const int c = k * 32 + lane;
-        e[k] = c < p.n_chunks ? crow[c] : make_float2(-INFINITY, 0.f);
+        e[k] = c < p.n_chunks ? __ldcg(crow + c) : make_float2(-INFINITY, 0.f);
       }
       // two passes: the row maximum, then each chunk's mass in units of 2^M
       // (the chunk search reuses the masses as its weights)
@@ -376,7 +379,7 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
 #pragma unroll
         for (int k = 0; k < KC; ++k) {
           const int i = k * 32 + lane;
-          f[k] = i < nsub ? p.fine[static_cast<size_t>(2 * tb + i) * p.R_pad + r] : make_float2(-INFINITY, 0.f);
+          f[k] = i < nsub ? __ldcg(p.fine + static_cast<size_t>(2 * tb + i) * p.R_pad + r) : make_float2(-INFINITY, 0.f);
         }
         __syncwarp();  // every lane is done reading the chunk weights
 #pragma unroll
@@ -651,7 +654,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
       if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
         int tok = -1;
         if (valid) {
-          tok = step == 0 ? p.anchors[r] : p.tokens[static_cast<size_t>(r) * p.gamma + step - 1];
+          tok = step == 0 ? p.anchors[r] : __ldcg(p.tokens + static_cast<size_t>(r) * p.gamma + step - 1);
           if (tok < 0 || tok >= p.V) {
             report(p.status, DSPARK_STATUS_BAD_TOKEN);
             tok = 0;
@@ -709,6 +712,9 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
             const float4 t4 = urow[k];
             z[4 * k] += t4.x; z[4 * k + 1] += t4.y; z[4 * k + 2] += t4.z; z[4 * k + 3] += t4.w;
           }
+          // the stage is refilled by TMA (async proxy) once released: order these
+          // generic-proxy reads before that write
+          fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_uempty + 8 * su);
 
@@ -788,6 +794,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
             *abort_flag = 1;
             break;
           }
+          __syncwarp();  // the other lanes' loads are ordered after lane 0's acquire
           sample_greedy(p, rr, step);
         }
       } else {

@@ -351,6 +351,9 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
         const float4 t4 = urow[k];
         u[4 * k] = t4.x; u[4 * k + 1] = t4.y; u[4 * k + 2] = t4.z; u[4 * k + 3] = t4.w;
       }
+      // the stage is refilled by bulk copies (async proxy) once released: order
+      // these generic-proxy reads before that write
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_uempty + 8 * s);
 
