@@ -145,3 +145,55 @@ def test_nonfinite_logits_reported():
     assert dr.status() & DSPARK_STATUS_NONFINITE
     tok = host(dr.tokens)
     assert tok.min() >= 0 and tok.max() < wl.V
+
+
+def test_one_graph_many_rounds_device_decided_lengths():
+    # One captured round replayed on new inputs: the scheduler decides each
+    # request's verify length on the device, and verify consumes those
+    # variable lengths inside the same graph; no length is baked into it.
+    wl = synth.scaled(synth.WORKLOADS["tiny_r4_g7_v4096"], R=16, gamma=6, V=4096, d=64, name="graph_lens")
+    dr, _ = device_round(wl)
+    W1, W2, w = weights(wl)
+
+    def load(rnd):
+        inp = synth.round_inputs(wl, rnd)
+        dr.set_round(inp.U, inp.h, inp.anchors)
+        dr.T.copy_(torch.from_numpy(_target(wl, inp, np.zeros((wl.R, wl.gamma), np.int32), rnd)))
+
+    def run():
+        dr.draft(1.0, wl.seed, 0)
+        dr.confidence()
+        dr.schedule(MODE_EARLY_STOP)
+        dr.verify(1.0, wl.seed, 0)
+
+    outs = (dr.tokens, dr.a, dr.lens, dr.sched_out, dr.n_accept, dr.next_token)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    load(0)
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run()
+    lens_seen = []
+    for rnd in range(3):
+        load(rnd)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            run()
+        torch.cuda.synchronize()
+        eager = [host(x).copy() for x in outs]
+        for x in outs:
+            x.zero_()
+        load(rnd)
+        g.replay()
+        torch.cuda.synchronize()
+        replay = [host(x) for x in outs]
+        for e, r in zip(eager, replay):
+            assert np.array_equal(e, r)
+        lens_seen.append(tuple(replay[2][: wl.R]))
+        assert int(replay[3][0]) == int(np.sum(replay[2][: wl.R]))
+        assert np.all(replay[4][: wl.R] <= replay[2][: wl.R])
+    assert len(set(lens_seen)) > 1  # the lengths really are decided per replay
+    assert dr.status() == 0
