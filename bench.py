@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per dspark_markov_draft call (one round's 16 positions) from the
 # ncu capture summarised in profiles/; valid only for the draft kernel sources
 # whose digest (draft_digest) is recorded with it.
-NCU_DRAFT_TRAFFIC = {"digest": "a4ec736d5a8a", "bytes_per_call": 1.91e9 + 50.23e6}
+NCU_DRAFT_TRAFFIC = {"digest": "5660a414388c", "bytes_per_call": 1.92e9 + 52.36e6}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -375,6 +375,12 @@ def run_gpu(args):
     traffic = NCU_DRAFT_TRAFFIC["bytes_per_call"] if NCU_DRAFT_TRAFFIC["digest"] == draft_digest() else None
 
     # ------------------------------------------------------------- end to end (host buffers)
+    # Every step copies the round's inputs in from pinned host memory and reads
+    # its results back.  Verify reads only target rows 0..lens[r] of request r,
+    # and those lengths are decided on the device by the scheduler: the step
+    # reads them back (R int32) after the schedule and copies in just those
+    # target rows, as a serving loop that evaluates only the scheduled
+    # positions would.
     e2e = None
     if not args.no_e2e:
         hU = torch.empty(dr.U.shape, dtype=dr.U.dtype, pin_memory=True)
@@ -385,24 +391,46 @@ def run_gpu(args):
         hh.copy_(dr.h)
         outs = [dr.tokens, dr.n_accept, dr.next_token]
         hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        hlens = torch.empty(dr.lens.shape, dtype=dr.lens.dtype, pin_memory=True)
         n_e2e = max(1, min(args.steps, 10))
+        t_rows = []
+
+        def e2e_step():
+            dr.U.copy_(hU, non_blocking=True)
+            dr.h.copy_(hh, non_blocking=True)
+            calls[0]()  # draft
+            calls[1]()  # confidence
+            calls[2]()  # schedule
+            hlens.copy_(dr.lens, non_blocking=True)
+            stream.synchronize()
+            rows = 0
+            for r in range(R):
+                n = int(hlens[r]) + 1
+                dr.T[r, :n].copy_(hT[r, :n], non_blocking=True)
+                rows += n
+            calls[3]()  # verify
+            for o, ho in zip(outs, hout):
+                ho.copy_(o, non_blocking=True)
+            stream.synchronize()
+            return rows
+
+        with torch.cuda.stream(stream):
+            for _ in range(2):  # untimed
+                e2e_step()
         torch.cuda.synchronize()
         barrier(world, device)
         t0 = time.perf_counter()
         with torch.cuda.stream(stream):
             for _ in range(n_e2e):
-                dr.U.copy_(hU, non_blocking=True)
-                dr.T.copy_(hT, non_blocking=True)
-                dr.h.copy_(hh, non_blocking=True)
-                for f in calls:
-                    f()
-                for o, ho in zip(outs, hout):
-                    ho.copy_(o, non_blocking=True)
-                stream.synchronize()
+                t_rows.append(e2e_step())
         t_e2e = max_over_ranks(time.perf_counter() - t0, world, device)
+        mean_rows = sum(t_rows) / len(t_rows)
         e2e = {"value": tokens_per_step * world * n_e2e / t_e2e, "unit": "tokens/s",
-               "h2d_bytes_per_step": int(hU.numel() * 4 + hT.numel() * 4 + hh.numel() * 2),
-               "d2h_bytes_per_step": int(sum(o.numel() * o.element_size() for o in outs)), "steps": n_e2e}
+               "h2d_bytes_per_step": int(hU.numel() * 4 + hh.numel() * 2 + mean_rows * V * 4),
+               "d2h_bytes_per_step": int(sum(o.numel() * o.element_size() for o in outs) + hlens.numel() * 4),
+               "steps": n_e2e,
+               "note": "U and h in every step; target rows in for the verified positions only (their number is "
+                       "decided on the device and read back after the schedule)"}
 
     # ------------------------------------------------------------- CPU oracle on a bounded sample
     cpu = None

@@ -44,6 +44,12 @@ struct WorkspaceLayout {
   // each on its own 64-byte line.  Zeroed at the start of every draft call.
   size_t dsync = 0;
   size_t dsync_bytes = 0;
+  // The draft's staging copy of each row's next A operand (the W1 row of the
+  // token just drawn), 512 bytes per row, in the same unused tail, laid out so
+  // that a gather warp reads whole 128-byte lines: uint4 index
+  // (((mtile * 4 + quarter) * 2 + half) * 16 + k) * 32 + lane.
+  size_t abuf = 0;
+  size_t abuf_bytes = 0;
 };
 
 inline WorkspaceLayout workspace_layout(int R, int gamma, int V) {
@@ -63,6 +69,8 @@ inline WorkspaceLayout workspace_layout(int R, int gamma, int V) {
   L.total = off;
   L.dsync = L.coarse + R_pad * kMaxSampleChunks * 8;
   L.dsync_bytes = 64 * (2 * (R_pad / kMTile) + 1);
+  L.abuf = align256(L.dsync + L.dsync_bytes);
+  L.abuf_bytes = R_pad * 512;
   return L;
 }
 

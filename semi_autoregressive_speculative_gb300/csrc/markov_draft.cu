@@ -67,6 +67,7 @@ struct DraftArgs {
   uint32_t* done;          // [n_mtiles] CTAs that finished a position, 16 words apart
   uint32_t* ready;         // [n_mtiles] tokens published, 16 words apart
   uint32_t* abort;         // any CTA gave up on a wait
+  uint4* abuf;             // each row's next A operand (W1 row of its last token), gather-ordered
   int R, R_pad, gamma, V, rank, n_tiles, n_chunks, n_mtiles;
   float scale;             // log2(e) / T (1 when greedy)
   uint64_t seed;
@@ -238,13 +239,19 @@ __device__ __forceinline__ float tree_argmax32(const float (&z)[32], int* idx) {
   return t[0];
 }
 
-// Counts request r's token as published on its M-tile after bringing the next
-// position's W1 row into L2 (one warp; lane 0 counts).
+// Publishes request r's token x (one warp): copies W1[x] into the row's slot
+// of the A-operand staging buffer, in the order the gather reads it (for each
+// 16-byte piece k, the 32 rows of a lane quarter are contiguous, so a gather
+// warp reads whole 128-byte lines), then lane 0 counts the token on the M-tile.
 __device__ __forceinline__ void publish_token(const DraftArgs& p, int r, int step, int x) {
   if (step + 1 >= p.gamma) return;
   const int lane = threadIdx.x & 31;
-  if (lane * 128 < p.rank * 2)
-    prefetch_l2(reinterpret_cast<const uint8_t*>(p.W1 + static_cast<size_t>(x) * p.rank) + lane * 128);
+  const int half_u4 = p.rank / 16;  // uint4 per half row; a row is 2 * half_u4 <= 32 of them
+  if (lane < 2 * half_u4) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(x) * p.rank) + lane);
+    const int rr = r % kMTile, h = lane / half_u4, k = lane - h * half_u4;
+    p.abuf[((((static_cast<size_t>(r / kMTile) * 4 + (rr >> 5)) * 2 + h) * 16 + k) << 5) + (rr & 31)] = v;
+  }
   __syncwarp();
   if (lane == 0) {
     __threadfence();
@@ -652,22 +659,33 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
         named_barrier(4, kEpiThreads);
       }
       if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
-        int tok = -1;
-        if (valid) {
-          tok = step == 0 ? p.anchors[r] : __ldcg(p.tokens + static_cast<size_t>(r) * p.gamma + step - 1);
-          if (tok < 0 || tok >= p.V) {
-            report(p.status, DSPARK_STATUS_BAD_TOKEN);
-            tok = 0;
-          }
-        }
-        const uint4* src =
-            reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(tok < 0 ? 0 : tok) * p.rank) + h * half_u4;
         uint32_t a[64];  // all loads first, then the tensor-memory stores
+        if (step == 0) {
+          int tok = -1;
+          if (valid) {
+            tok = p.anchors[r];
+            if (tok < 0 || tok >= p.V) {
+              report(p.status, DSPARK_STATUS_BAD_TOKEN);
+              tok = 0;
+            }
+          }
+          const uint4* src =
+              reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(tok < 0 ? 0 : tok) * p.rank) + h * half_u4;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          uint4 wv = make_uint4(0, 0, 0, 0);
-          if (tok >= 0 && k < half_u4) wv = __ldg(src + k);
-          a[4 * k] = wv.x; a[4 * k + 1] = wv.y; a[4 * k + 2] = wv.z; a[4 * k + 3] = wv.w;
+          for (int k = 0; k < 16; ++k) {
+            uint4 wv = make_uint4(0, 0, 0, 0);
+            if (tok >= 0 && k < half_u4) wv = __ldg(src + k);
+            a[4 * k] = wv.x; a[4 * k + 1] = wv.y; a[4 * k + 2] = wv.z; a[4 * k + 3] = wv.w;
+          }
+        } else {
+          // the staged W1 rows of this M-tile's previous tokens (written by other CTAs: through L2)
+          const uint4* src = p.abuf + ((((static_cast<size_t>(mtile) * 4 + q) * 2 + h) * 16) << 5) + lane;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            uint4 wv = make_uint4(0, 0, 0, 0);
+            if (valid && k < half_u4) wv = __ldcg(src + (k << 5));
+            a[4 * k] = wv.x; a[4 * k + 1] = wv.y; a[4 * k + 2] = wv.z; a[4 * k + 3] = wv.w;
+          }
         }
         const uint32_t dst = tmem_a + lane_off + static_cast<uint32_t>(h * 4 * half_u4);
         const uint32_t(&a0)[32] = *reinterpret_cast<const uint32_t(*)[32]>(&a[0]);
@@ -902,6 +920,7 @@ int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
   a.done = reinterpret_cast<uint32_t*>(ws + L.dsync);
   a.ready = a.done + 16 * a.n_mtiles;
   a.abort = a.ready + 16 * a.n_mtiles;
+  a.abuf = reinterpret_cast<uint4*>(ws + L.abuf);
   a.R_pad = a.n_mtiles * kMTile;
   a.gamma = gamma; a.V = V; a.rank = rank;
   a.n_tiles = ceil_div(V, kTileN);

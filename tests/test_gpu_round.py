@@ -153,6 +153,9 @@ def test_one_graph_many_rounds_device_decided_lengths():
     # variable lengths inside the same graph; no length is baked into it.
     wl = synth.scaled(synth.WORKLOADS["tiny_r4_g7_v4096"], R=16, gamma=6, V=4096, d=64, name="graph_lens")
     dr, _ = device_round(wl)
+    # a throughput curve with cliffs inside this batch, so that early stop
+    # admits a different set of positions for different confidences
+    dr.sps.copy_(torch.from_numpy(_staircase_scaled(wl)))
     W1, W2, w = weights(wl)
 
     def load(rnd):
