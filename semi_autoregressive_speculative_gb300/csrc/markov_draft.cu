@@ -61,10 +61,9 @@ struct DraftArgs {
   int32_t* tokens;         // [R, gamma]
   float* pd_tok;           // [R, gamma]
   float* logZ;             // [R, gamma]
-  float2* coarse;          // [R_pad][n_chunks]
+  unsigned long long* centry;  // [R_pad][n_chunks] tagged chunk entries (see chunk_entry)
   float2* fine;            // [2 * n_tiles][R_pad]
   int32_t* status;
-  uint32_t* done;          // [n_mtiles] CTAs that finished a position, 16 words apart
   uint32_t* ready;         // [n_mtiles] tokens published, 16 words apart
   uint32_t* abort;         // any CTA gave up on a wait
   uint4* abuf;             // each row's next A operand (W1 row of its last token), gather-ordered
@@ -103,6 +102,14 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
   uint32_t v;
@@ -259,22 +266,77 @@ __device__ __forceinline__ void publish_token(const DraftArgs& p, int r, int ste
   }
 }
 
-// Greedy sampler for request r (one warp, every chunk partial of its M-tile
-// visible): the argmax of the chunk partials, lowest index on ties.  Partials
+// A chunk's partial for one row, published by its CTA in one 64-bit release
+// store: the low word is a float (sampled: the chunk's log2-sum-exp2
+// L = max + log2(sum), greedy: its maximum), the high word carries the
+// position tag (position + 1) in its top 8 bits and, greedy, the argmax in its
+// low 24 bits.  The samplers poll their row's entries directly: no CTA count,
+// and each chunk is folded in as soon as it lands.  Entries are zeroed at the
+// start of every call, so a tag from an earlier call never matches.
+__device__ __forceinline__ unsigned long long chunk_entry(float lo, uint32_t tag, uint32_t idx) {
+  return (static_cast<unsigned long long>((tag << 24) | idx) << 32) | __float_as_uint(lo);
+}
+
+constexpr int kEntriesPerLane = kMaxSampleChunks / 32;
+
+// One warp waits until every chunk entry of row r carries `tag`; lane l gets
+// the entries of chunks k * 32 + l in e[k] (0 past n_chunks).  Polls with an
+// acquire load per pending entry and a short sleep; gives up (false, the same
+// in every lane, abort word raised) after kWaitLimitNs or on abort.
+__device__ __forceinline__ bool poll_row(const DraftArgs& p, int r, uint32_t tag,
+                                         unsigned long long (&e)[kEntriesPerLane]) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long* row = p.centry + static_cast<size_t>(r) * p.n_chunks;
+  uint32_t pending = 0;
+#pragma unroll
+  for (int k = 0; k < kEntriesPerLane; ++k) {
+    e[k] = 0ull;
+    if (k * 32 + lane < p.n_chunks) pending |= 1u << k;
+  }
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+#pragma unroll
+    for (int k = 0; k < kEntriesPerLane; ++k) {
+      if (pending & (1u << k)) {
+        const unsigned long long v = ld_acquire_gpu_u64(row + k * 32 + lane);
+        if (static_cast<uint32_t>(v >> 56) == tag) {
+          e[k] = v;
+          pending &= ~(1u << k);
+        }
+      }
+    }
+    if (__all_sync(0xffffffffu, pending == 0)) break;
+    if ((it & 15u) == 15u) {
+      int bad = 0;
+      if (lane == 0) bad = ld_relaxed_gpu(p.abort) != 0 || global_ns() - t0 > kWaitLimitNs;
+      if (__shfl_sync(0xffffffffu, bad, 0)) {
+        if (lane == 0) atomicExch(p.abort, 1u);
+        return false;
+      }
+    }
+    __nanosleep(32);
+  }
+  __syncwarp();  // every lane's later loads are ordered after all the acquires
+  return true;
+}
+
+// Greedy sampler for request r (one warp): waits for every chunk entry of the
+// row, then takes the argmax, lowest index on ties.  False when the wait gave up.  Partials
 // and tokens that other CTAs write during the call are read through L2
 // (ld.global.cg): this SM's L1 may hold the previous position's lines.
-__device__ __forceinline__ void sample_greedy(const DraftArgs& p, int r, int step) {
+__device__ __forceinline__ bool sample_greedy(const DraftArgs& p, int r, int step) {
   const int lane = threadIdx.x & 31;
   const size_t out = static_cast<size_t>(r) * p.gamma + step;
-  const float2* crow = p.coarse + static_cast<size_t>(r) * p.n_chunks;
+  unsigned long long ent[kEntriesPerLane];
+  if (!poll_row(p, r, static_cast<uint32_t>(step + 1), ent)) return false;
   float best = -INFINITY;
   int bidx = 0x7fffffff;
 #pragma unroll
-  for (int k = 0; k < kMaxSampleChunks / 32; ++k) {
-    const int c = k * 32 + lane;
-    const float2 e = c < p.n_chunks ? __ldcg(crow + c) : make_float2(-INFINITY, 0.f);
-    const int ei = __float_as_int(e.y);
-    if (e.x > best || (e.x == best && e.x > -INFINITY && ei < bidx)) { best = e.x; bidx = ei; }
+  for (int k = 0; k < kEntriesPerLane; ++k) {
+    if (k * 32 + lane >= p.n_chunks) continue;
+    const float ex = __uint_as_float(static_cast<uint32_t>(ent[k]));
+    const int ei = static_cast<int>((ent[k] >> 32) & 0xFFFFFFu);
+    if (ex > best || (ex == best && ex > -INFINITY && ei < bidx)) { best = ex; bidx = ei; }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -292,6 +354,7 @@ __device__ __forceinline__ void sample_greedy(const DraftArgs& p, int r, int ste
     p.logZ[out] = best;
   }
   publish_token(p, r, step, bidx);
+  return true;
 }
 
 // What the leader warp hands to the other sampling warps of its CTA.
@@ -342,32 +405,31 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
 
   if (sub == 0) {
     const float u = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(step), kDraftSample);
-    bool ok = true;
-    if (lane == 0)
-      ok = wait_at_least(p.done + 16 * (r / kMTile), static_cast<uint32_t>(p.n_chunks * (step + 1)), p.abort);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();  // the other lanes' loads below are ordered after lane 0's acquire
+    constexpr int KC = kEntriesPerLane;
+    unsigned long long ent[KC];
+    const bool ok = poll_row(p, r, static_cast<uint32_t>(step + 1), ent);
     int state = kSlotAbort, sstar = 0;
     float M = 0.f, Z = 0.f, target = 0.f, before_s = 0.f;
     if (ok) {
-      constexpr int KC = kMaxSampleChunks / 32;
-      const float2* crow = p.coarse + static_cast<size_t>(r) * p.n_chunks;
-      float2 e[KC];
+      // each chunk's log2-sum-exp2; chunks past n_chunks count as empty
+      float L[KC];
 #pragma unroll
-      for (int k = 0; k < KC; ++k) {
-        const int c = k * 32 + lane;
-        e[k] = c < p.n_chunks ? __ldcg(crow + c) : make_float2(-INFINITY, 0.f);
-      }
+      for (int k = 0; k < KC; ++k)
+        L[k] = k * 32 + lane < p.n_chunks ? __uint_as_float(static_cast<uint32_t>(ent[k])) : -INFINITY;
       // two passes: the row maximum, then each chunk's mass in units of 2^M
       // (the chunk search reuses the masses as its weights)
       float m = -INFINITY;
+      bool nan_seen = false;
 #pragma unroll
-      for (int k = 0; k < KC; ++k) m = fmaxf(m, e[k].x);
-      M = warp_max(m);
+      for (int k = 0; k < KC; ++k) {
+        m = fmaxf(m, L[k]);
+        nan_seen |= L[k] != L[k];
+      }
+      M = __any_sync(0xffffffffu, nan_seen) ? NAN : warp_max(m);
       float zs = 0.f;
 #pragma unroll
       for (int k = 0; k < KC; ++k) {
-        const float wk = e[k].x > -INFINITY ? e[k].y * ex2(e[k].x - M) : 0.f;
+        const float wk = L[k] > -INFINITY ? ex2(L[k] - M) : 0.f;
         sm.wts[k * 32 + lane] = wk;
         zs += wk;
       }
@@ -776,12 +838,14 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
       if (h == 1) s_half[row] = kGreedy ? make_float2(runM, __int_as_float(runIdx)) : make_float2(runM, runS);
       named_barrier(1, kEpiThreads);
       if (h == 0 && valid && !*abort_flag) {
+        // publish the row's chunk entry: one release store, after the barrier
+        // above has made both halves' sub-tile partials part of this thread's view
         const float2 o = s_half[row];
-        float2 outv;
+        unsigned long long ent;
         if constexpr (kGreedy) {
           const int oi = __float_as_int(o.y);
           if (o.x > runM || (o.x == runM && oi < runIdx)) { runM = o.x; runIdx = oi; }
-          outv = make_float2(runM, __int_as_float(runIdx));
+          ent = chunk_entry(runM, static_cast<uint32_t>(step + 1), static_cast<uint32_t>(runIdx));
         } else {
           const float Mx = fmaxf(runM, o.x);
           float S = 0.f;
@@ -789,31 +853,21 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
             if (runM > -INFINITY) S += runS * ex2(runM - Mx);
             if (o.x > -INFINITY) S += o.y * ex2(o.x - Mx);
           }
-          outv = make_float2(Mx, S);
+          // a NaN sum stays NaN in L, so that the sampler reports the row
+          const float L = Mx > -INFINITY ? Mx + __log2f(S) : -INFINITY;
+          ent = chunk_entry(L, static_cast<uint32_t>(step + 1), 0u);
         }
-        p.coarse[static_cast<size_t>(r) * p.n_chunks + chunk] = outv;
-      }
-      // ---- this CTA is done with the position: count it on its M-tile
-      named_barrier(3, kEpiThreads);
-      if (threadIdx.x == 64 && !*abort_flag) {
-        __threadfence();
-        atomicAdd(p.done + 16 * mtile, 1u);
+        st_release_gpu_u64(p.centry + static_cast<size_t>(r) * p.n_chunks + chunk, ent);
       }
 
       // ---- sample this CTA's requests once every chunk of their M-tile is done
       if constexpr (kGreedy) {
         // one warp per request
         for (int rr = blockIdx.x + gridDim.x * (warp - 2); rr < p.R; rr += gridDim.x * (kEpiThreads / 32)) {
-          bool ok = true;
-          if (lane == 0)
-            ok = !*abort_flag && wait_at_least(p.done + 16 * (rr / kMTile),
-                                               static_cast<uint32_t>(p.n_chunks * (step + 1)), p.abort);
-          if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          if (__any_sync(0xffffffffu, *abort_flag != 0) || !sample_greedy(p, rr, step)) {
             *abort_flag = 1;
             break;
           }
-          __syncwarp();  // the other lanes' loads are ordered after lane 0's acquire
-          sample_greedy(p, rr, step);
         }
       } else {
         // all 8 epilogue warps on each of this CTA's requests in turn
@@ -912,13 +966,12 @@ int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
   DraftArgs a = {};
   a.U = U; a.W1 = W1; a.W2 = W2; a.anchors = anchors;
   a.tokens = tokens; a.pd_tok = pd_tok; a.logZ = logZ;
-  a.coarse = reinterpret_cast<float2*>(ws + L.coarse);
+  a.centry = reinterpret_cast<unsigned long long*>(ws + L.coarse);
   a.fine = reinterpret_cast<float2*>(ws + L.fine);
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
   a.R = R;
   a.n_mtiles = ceil_div(R, kMTile);
-  a.done = reinterpret_cast<uint32_t*>(ws + L.dsync);
-  a.ready = a.done + 16 * a.n_mtiles;
+  a.ready = reinterpret_cast<uint32_t*>(ws + L.dsync) + 16 * a.n_mtiles;
   a.abort = a.ready + 16 * a.n_mtiles;
   a.abuf = reinterpret_cast<uint4*>(ws + L.abuf);
   a.R_pad = a.n_mtiles * kMTile;
@@ -943,8 +996,11 @@ int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
   auto kernel = greedy ? k_markov_draft<true> : k_markov_draft<false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess)
     return DSPARK_ERR_CUDA;
-  // done / ready counters and the abort word start at zero on every call
-  if (cudaMemsetAsync(ws + L.dsync, 0, L.dsync_bytes, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  // the chunk entries (no tag matches), the ready counters and the abort word
+  // start at zero on every call
+  if (cudaMemsetAsync(ws + L.coarse, 0, static_cast<size_t>(a.R_pad) * a.n_chunks * 8, stream) != cudaSuccess ||
+      cudaMemsetAsync(ws + L.dsync, 0, L.dsync_bytes, stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks * a.n_mtiles);
