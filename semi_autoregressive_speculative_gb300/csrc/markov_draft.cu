@@ -195,6 +195,11 @@ __device__ __forceinline__ Crossing warp_crossing(const float* w, int n, float b
   return c;
 }
 
+// The i-th tile a CTA sweeps at position `step`: forwards at even positions,
+// backwards at odd ones, so that the W2 tiles a position uses last (the most
+// recently used in L2) are the first the next position needs.
+__device__ __forceinline__ int tile_of(int step, int i, int ntile) { return (step & 1) ? ntile - 1 - i : i; }
+
 // First 64-column tile of chunk c when n_tiles tiles are split into n_chunks
 // contiguous chunks.  32-bit: c <= kMaxSampleChunks and n_tiles < 2^18 (the
 // host limits V to 2^24), so c * n_tiles < 2^26.
@@ -622,7 +627,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
       int wfilled = 0, ufilled = 0;
       for (int it = 0; it < total_tiles; ++it) {
         const int step = it / ntile;
-        const int v0 = (t_begin + (it - step * ntile)) * kTileN;
+        const int v0 = (t_begin + tile_of(step, it - step * ntile, ntile)) * kTileN;
         const int sw = it % kDraftWStages, su = it % kDraftUStages;
         if (!mbar_wait(bar_wempty + 8 * sw, ((it / kDraftWStages) & 1) ^ 1, abort_flag)) {
           *abort_flag = 1;
@@ -799,19 +804,20 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
           if (lane == 0) mbar_arrive(bar_uempty + 8 * su);
 
           // z = bias + U of 32 columns; columns past V only in the last tile
-          const int v0 = (t_begin + i) * kTileN + h * kSubN;
+          const int ti = tile_of(step, i, ntile);  // this tile's place in the chunk
+          const int v0 = (t_begin + ti) * kTileN + h * kSubN;
           const int ncol = min(kSubN, p.V - v0);
           if (ncol < kSubN) {
 #pragma unroll
             for (int k = 0; k < 32; ++k) z[k] = k < ncol ? z[k] : -INFINITY;
           }
-          const size_t fidx = static_cast<size_t>(2 * (t_begin + i) + h) * p.R_pad + r;
+          const size_t fidx = static_cast<size_t>(2 * (t_begin + ti) + h) * p.R_pad + r;
           if constexpr (kGreedy) {
             int k;
             const float mx = tree_argmax32(z, &k);
             const int ix = v0 + k;
             if (valid) p.fine[fidx] = make_float2(mx, __int_as_float(ix));
-            if (mx > runM) { runM = mx; runIdx = ix; }
+            if (mx > runM || (mx == runM && ix < runIdx)) { runM = mx; runIdx = ix; }
           } else {
             // y = z * log2(e)/T; partial (max y, sum exp2(y - max y))
             const float mz = tree_max32(z);
