@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per dspark_markov_draft call (one round's 16 positions) from the
 # ncu capture summarised in profiles/; valid only for the draft kernel sources
 # whose digest (draft_digest) is recorded with it.
-NCU_DRAFT_TRAFFIC = {"digest": "600a5488f520", "bytes_per_call": 1.61e9 + 20.67e6}
+NCU_DRAFT_TRAFFIC = {"digest": "39419d47715a", "bytes_per_call": 1.60e9 + 23.84e6}
 
 
 # ----------------------------------------------------------------------------- helpers

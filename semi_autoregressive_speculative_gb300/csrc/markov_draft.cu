@@ -9,7 +9,8 @@
 //            (one 128-row x 64-column box per tile: 256 contiguous bytes per
 //            row, which is what lets the HBM stream run near its peak) come
 //            in through TMA rings; tcgen05.mma into fp32 accumulators in
-//            tensor memory; the epilogue adds U, scales by log2(e)/T and
+//            tensor memory, two tiles per instruction (below); the epilogue
+//            adds U, scales by log2(e)/T and
 //            reduces each 32-column sub-tile and the whole chunk to softmax
 //            partials (max, sum exp2) — (max, argmax) when greedy.  Logits
 //            never reach HBM.  The CTA then counts itself done on its M-tile.
@@ -40,8 +41,25 @@
 
 namespace dspark {
 
-constexpr int kDraftWStages = 3;  // W2 tiles in flight per CTA (L2-resident after the first position)
-constexpr int kDraftUStages = 3;  // U tiles in flight per CTA (the HBM stream)
+// Tiles are multiplied in pairs.  An M=128, K=16 tcgen05.mma costs about the
+// same time at N=64 as at N=128 (about 100 cycles: the tensor pipe is bound
+// by the instruction, not by its N), so one N=128 instruction per K-step
+// covers two 64-column tiles and halves the tensor time per tile.
+// W2 comes in K-chunks: a ring stage holds 64 rank rows of both tiles of a
+// pair (two 64 x 64 boxes, 128-byte swizzled, 8 KB apart: the B descriptor
+// spans them as two swizzle atoms along N).  A stage is released as soon as
+// its 4 MMAs are done, so the ring keeps most of its bytes in flight.
+constexpr int kDraftKChunk = 64;     // rank rows per W2 stage
+constexpr int kDraftWBox = kDraftKChunk * 128;  // bytes of one 64-column box of a stage
+constexpr int kDraftWStages = 6;     // W2 K-chunk stages (L2-resident after the first position)
+constexpr int kDraftUStages = 3;     // U tiles in flight per CTA (the HBM stream)
+constexpr int kDraftAccPairs = 3;    // fp32 accumulator pairs (2 x 64 columns each) in tensor memory
+constexpr int kDraftACol = kDraftAccPairs * 2 * kTileN;  // first tensor-memory column of the A operand
+constexpr int kDraftTmemCols = 512;                      // accumulators + A (rank / 2 <= 128 columns)
+static_assert(kDraftACol + 128 <= kDraftTmemCols, "tensor-memory plan");
+// warp 0 W2 producer, warp 1 MMA issuer, warps 2..9 epilogue and samplers, warp 10 U producer
+constexpr int kDraftKThreads = kDraftThreads + 32;
+constexpr int kUWarp = 10;
 // A U tile is one 128-row x 68-column box: the 64 columns of the tile plus the
 // first 4 of the next.  Each request row is one 272-byte run in HBM (runs of
 // 256 bytes and more keep the stream near the copy rate; 128-byte runs lose
@@ -84,7 +102,7 @@ struct DraftSmem {
 __host__ __device__ inline DraftSmem draft_smem_plan(int rank) {
   DraftSmem s;
   uint32_t off = 0;
-  s.w0 = off; s.wstride = 128u * rank; off += kDraftWStages * s.wstride;  // rank x 64 bf16, SW128
+  s.w0 = off; s.wstride = 2u * kDraftWBox; off += kDraftWStages * s.wstride;  // 2 x (64 rows x 64 bf16), SW128
   s.u0 = off; off += kDraftUStages * kDraftUBytes;
   s.half = off; off += kMTile * 8;
   s.bars = off; off += 256;
@@ -555,8 +573,42 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
   return state == kSlotAbort ? -1 : (state == kSlotSample ? 1 : 0);
 }
 
+// Adds tile `it`'s U values (this thread's row, 32 columns of half h) to z
+// once the tile's U stage has landed, then releases the stage.  False when the
+// wait gave up.
+__device__ __forceinline__ bool add_u_tile(float (&z)[32], uint32_t bar_ufull, uint32_t bar_uempty, const uint8_t* u0,
+                                           int row, int h, int it, volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  const int su = it % kDraftUStages;
+  if (!__all_sync(0xffffffffu, mbar_wait(bar_ufull + 8 * su, (it / kDraftUStages) & 1, abort_flag))) return false;
+  const float4* urow = reinterpret_cast<const float4*>(u0 + su * kDraftUBytes + row * (kDraftUCols * 4) + h * (kSubN * 4));
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float4 t4 = urow[k];
+    z[4 * k] += t4.x; z[4 * k + 1] += t4.y; z[4 * k + 2] += t4.z; z[4 * k + 3] += t4.w;
+  }
+  // the stage is refilled by TMA (async proxy) once released: order these
+  // generic-proxy reads before that write
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar_uempty + 8 * su);
+  return true;
+}
+
+// Folds a sub-tile partial (max y, sum exp2(y - max y)) into a running one.
+__device__ __forceinline__ void merge_partial(float mx, float sm, float& runM, float& runS) {
+  if (mx > -INFINITY) {
+    if (mx > runM) {
+      runS = (runM > -INFINITY ? runS * ex2(runM - mx) : 0.f) + sm;
+      runM = mx;
+    } else {
+      runS += sm * ex2(mx - runM);
+    }
+  }
+}
+
 template <bool kGreedy>
-__global__ void __launch_bounds__(kDraftThreads, 1)
+__global__ void __launch_bounds__(kDraftKThreads, 1)
     k_markov_draft(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u,
                    const __grid_constant__ CUtensorMap tm_slab, const DraftArgs p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -579,10 +631,11 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
   const uint32_t bar_wempty = bar_wfull + 8 * kDraftWStages;  // [kDraftWStages]
   const uint32_t bar_ufull = bar_wempty + 8 * kDraftWStages;  // [kDraftUStages]
   const uint32_t bar_uempty = bar_ufull + 8 * kDraftUStages;  // [kDraftUStages]
-  const uint32_t bar_tfull = bar_uempty + 8 * kDraftUStages;  // [2]
-  const uint32_t bar_tempty = bar_tfull + 16;                 // [2]
-  const uint32_t bar_slab = bar_tempty + 16;                  // the sampler's slab copies
-  constexpr uint32_t kBarBytes = 16 * (kDraftWStages + kDraftUStages) + 40;
+  const uint32_t bar_tfull = bar_uempty + 8 * kDraftUStages;   // [kDraftAccPairs]
+  const uint32_t bar_tempty = bar_tfull + 8 * kDraftAccPairs;  // [kDraftAccPairs]
+  const uint32_t bar_slab = bar_tempty + 8 * kDraftAccPairs;   // the sampler's slab copies
+  const uint32_t bar_drain = bar_slab + 8;                     // the MMA issuer's last commit on abort
+  constexpr uint32_t kBarBytes = 16 * (kDraftWStages + kDraftUStages + kDraftAccPairs) + 16;
   static_assert(kBarBytes + 8 <= 256, "barrier block");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + plan.bars + kBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + plan.bars + kBarBytes + 4);
@@ -597,11 +650,12 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
       mbar_init(bar_ufull + 8 * s, 1);
       mbar_init(bar_uempty + 8 * s, 8);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kDraftAccPairs; ++s) {
       mbar_init(bar_tfull + 8 * s, 1);
       mbar_init(bar_tempty + 8 * s, 8);
     }
     mbar_init(bar_slab, 1);
+    mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tm_w2);
@@ -609,33 +663,68 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
     prefetch_tensormap(&tm_slab);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_alloc(smem_u32(tmem_slot), kDraftTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t tmem_a = tmem_base + kAccCols;  // A operand columns
+  const uint32_t tmem_a = tmem_base + kDraftACol;  // A operand columns
+  // tile i of a position belongs to pair i / 2; pair gp of the call uses
+  // accumulator pair gp % kDraftAccPairs and W2 K-chunks g = gp * nkc + kc,
+  // in ring stage g % kDraftWStages
+  const int npair = (ntile + 1) >> 1;
+  const int nkc = p.rank / kDraftKChunk;
 
   if (warp == 0) {
-    // ---------------------------------------------------------- TMA producer (all positions, lane 0)
+    // ---------------------------------------------------------- W2 producer (all positions, lane 0)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_last();
+      uint32_t wlast = 0;  // per stage s: bit 2s = filled, bit 2s + 1 = parity of its last fill
+      bool ok = true;
+      for (int step = 0; step < p.gamma && ok; ++step) {
+        for (int j = 0; j < npair && ok; ++j) {
+          const int gp = step * npair + j;
+          const bool two = 2 * j + 1 < ntile;
+          const int va = (t_begin + tile_of(step, 2 * j, ntile)) * kTileN;
+          const int vb = two ? (t_begin + tile_of(step, 2 * j + 1, ntile)) * kTileN : 0;
+          for (int kc = 0; kc < nkc; ++kc) {
+            const int g = gp * nkc + kc;
+            const int sw = g % kDraftWStages;
+            const uint32_t par = static_cast<uint32_t>(g / kDraftWStages) & 1u;
+            if (!mbar_wait(bar_wempty + 8 * sw, par ^ 1u, abort_flag)) {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            // rows [kc * 64, kc * 64 + 64) of both tiles; columns past V are zero-filled
+            mbar_arrive_expect_tx(bar_wfull + 8 * sw, (two ? 2u : 1u) * kDraftWBox);
+            tma_load_2d(base + plan.w(sw), &tm_w2, bar_wfull + 8 * sw, va, kc * kDraftKChunk, pol_w);
+            if (two) tma_load_2d(base + plan.w(sw) + kDraftWBox, &tm_w2, bar_wfull + 8 * sw, vb, kc * kDraftKChunk, pol_w);
+            wlast = (wlast & ~(3u << (2 * sw))) | ((1u | (par << 1)) << (2 * sw));
+          }
+        }
+      }
+      if (*abort_flag) {
+        // let copies already in flight land before the CTA exits
+        const uint64_t t0 = global_ns();
+        for (int s = 0; s < kDraftWStages; ++s)
+          if ((wlast >> (2 * s)) & 1u)
+            while (!mbar_try_wait(bar_wfull + 8 * s, (wlast >> (2 * s + 1)) & 1u) && global_ns() - t0 < kWaitLimitNs) {
+            }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kUWarp) {
+    // ---------------------------------------------------------- U producer (all positions, lane 0)
+    if (lane == 0) {
       const uint64_t pol_u = policy_evict_first();
-      const uint32_t wbytes = 128u * p.rank;
-      int wfilled = 0, ufilled = 0;
+      int ufilled = 0;
       for (int it = 0; it < total_tiles; ++it) {
         const int step = it / ntile;
         const int v0 = (t_begin + tile_of(step, it - step * ntile, ntile)) * kTileN;
-        const int sw = it % kDraftWStages, su = it % kDraftUStages;
-        if (!mbar_wait(bar_wempty + 8 * sw, ((it / kDraftWStages) & 1) ^ 1, abort_flag)) {
-          *abort_flag = 1;
-          break;
-        }
-        mbar_arrive_expect_tx(bar_wfull + 8 * sw, wbytes);
-        tma_load_2d(base + plan.w(sw), &tm_w2, bar_wfull + 8 * sw, v0, 0, pol_w);
-        ++wfilled;
+        const int su = it % kDraftUStages;
         if (!mbar_wait(bar_uempty + 8 * su, ((it / kDraftUStages) & 1) ^ 1, abort_flag)) {
           *abort_flag = 1;
           break;
@@ -646,12 +735,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
         ++ufilled;
       }
       if (*abort_flag) {
-        // let copies already in flight land before the CTA exits
         const uint64_t t0 = global_ns();
-        for (int i = max(0, wfilled - kDraftWStages); i < wfilled; ++i)
-          while (!mbar_try_wait(bar_wfull + 8 * (i % kDraftWStages), (i / kDraftWStages) & 1) &&
-                 global_ns() - t0 < kWaitLimitNs) {
-          }
         for (int i = max(0, ufilled - kDraftUStages); i < ufilled; ++i)
           while (!mbar_try_wait(bar_ufull + 8 * (i % kDraftUStages), (i / kDraftUStages) & 1) &&
                  global_ns() - t0 < kWaitLimitNs) {
@@ -661,38 +745,52 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- UMMA issuer
-    const uint32_t idesc = idesc_bf16_f32(kMTile, kTileN, false, true);
-    const int ksteps = p.rank / 16;
-    int issued = 0;
+    const uint32_t idesc_pair = idesc_bf16_f32(kMTile, 2 * kTileN, false, true);
+    const uint32_t idesc_one = idesc_bf16_f32(kMTile, kTileN, false, true);
+    int issued = 0;  // any MMA issued
     for (int step = 0; step < p.gamma; ++step) {
       named_barrier(2, kEpiThreads + 32);  // this position's A operand is in tensor memory
       tc_fence_after_sync();
       if (lane == 0 && !*abort_flag) {
-        for (int i = 0; i < ntile; ++i) {
-          const int it = step * ntile + i;
-          const int sw = it % kDraftWStages, acc = it & 1;
-          if (!mbar_wait(bar_wfull + 8 * sw, (it / kDraftWStages) & 1, abort_flag) ||
-              !mbar_wait(bar_tempty + 8 * acc, ((it >> 1) & 1) ^ 1, abort_flag)) {
+        bool ok = true;
+        for (int j = 0; j < npair && ok; ++j) {
+          const int gp = step * npair + j, pa = gp % kDraftAccPairs;
+          if (!mbar_wait(bar_tempty + 8 * pa, ((gp / kDraftAccPairs) & 1) ^ 1, abort_flag)) {
             *abort_flag = 1;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
-          for (int ks = 0; ks < ksteps; ++ks) {
-            const uint32_t b_addr = base + plan.w(sw) + ks * 2048;
-            umma_bf16_ts(d, tmem_a + ks * 8, smem_desc_sw128(b_addr, 1024, 1024), idesc, ks > 0 ? 1u : 0u);
+          const uint32_t idesc = 2 * j + 1 < ntile ? idesc_pair : idesc_one;
+          const uint32_t d = tmem_base + static_cast<uint32_t>(pa * 2 * kTileN);
+          for (int kc = 0; kc < nkc; ++kc) {
+            const int g = gp * nkc + kc;
+            const int sw = g % kDraftWStages;
+            if (!mbar_wait(bar_wfull + 8 * sw, static_cast<uint32_t>(g / kDraftWStages) & 1u, abort_flag)) {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+#pragma unroll
+            for (int q4 = 0; q4 < kDraftKChunk / 16; ++q4) {
+              // N-direction atom stride (LBO) = one box: the pair's second tile
+              const uint32_t b_addr = base + plan.w(sw) + q4 * 2048;
+              const int ks = kc * (kDraftKChunk / 16) + q4;
+              umma_bf16_ts(d, tmem_a + ks * 8, smem_desc_sw128(b_addr, kDraftWBox, 1024), idesc, ks > 0 ? 1u : 0u);
+            }
+            umma_commit(bar_wempty + 8 * sw);
+            issued = 1;
           }
-          umma_commit(bar_wempty + 8 * sw);
-          umma_commit(bar_tfull + 8 * acc);
-          issued = it + 1;
+          if (ok) umma_commit(bar_tfull + 8 * pa);
         }
       }
       __syncwarp();
     }
     if (lane == 0 && *abort_flag && issued > 0) {
-      const int i = issued - 1;
+      // every MMA this thread issued is complete before tensor memory is freed
+      umma_commit(bar_drain);
       const uint64_t t0 = global_ns();
-      while (!mbar_try_wait(bar_tfull + 8 * (i & 1), (i >> 1) & 1) && global_ns() - t0 < kWaitLimitNs) {
+      while (!mbar_try_wait(bar_drain, 0) && global_ns() - t0 < kWaitLimitNs) {
       }
     }
   } else {
@@ -773,70 +871,82 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
       float runM = -INFINITY, runS = 0.f;  // running (max, sum exp2) of this warp's half of the chunk
       int runIdx = 0;                      // greedy: running argmax
       if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
-        for (int i = 0; i < ntile; ++i) {
-          const int it = step * ntile + i;
-          const int su = it % kDraftUStages, acc = it & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, (it >> 1) & 1, abort_flag))) {
+        // one pair of tiles per iteration: both accumulators are loaded
+        // together and the two tiles' arithmetic is interleaved
+        for (int j = 0; j < npair; ++j) {
+          const int i0 = 2 * j;
+          const bool two = i0 + 1 < ntile;
+          const int it0 = step * ntile + i0;
+          const int gp = step * npair + j, pa = gp % kDraftAccPairs;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * pa, (gp / kDraftAccPairs) & 1, abort_flag))) {
             *abort_flag = 1;
             break;
           }
           tc_fence_after_sync();
-          float z[32];
-          tmem_ld_32x32(tmem_base + lane_off + static_cast<uint32_t>(acc * kTileN + h * kSubN), z);
+          uint32_t a0[32], a1[32];
+          const uint32_t tacc = tmem_base + lane_off + static_cast<uint32_t>(2 * pa * kTileN + h * kSubN);
+          tmem_ld_32x32_nowait(tacc, a0);
+          tmem_ld_32x32_nowait(tacc + kTileN, a1);  // the second tile (not used when the pair has one)
+          tmem_wait_ld_tied(a0);
+          tmem_wait_ld_tied(a1);
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_ufull + 8 * su, (it / kDraftUStages) & 1, abort_flag))) {
+          if (lane == 0) mbar_arrive(bar_tempty + 8 * pa);
+          float z0[32], z1[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            z0[k] = __uint_as_float(a0[k]);
+            z1[k] = __uint_as_float(a1[k]);
+          }
+          if (!add_u_tile(z0, bar_ufull, bar_uempty, gbase + plan.u0, row, h, it0, abort_flag) ||
+              (two && !add_u_tile(z1, bar_ufull, bar_uempty, gbase + plan.u0, row, h, it0 + 1, abort_flag))) {
             *abort_flag = 1;
             break;
           }
-          const float4* urow =
-              reinterpret_cast<const float4*>(gbase + plan.u(su) + row * (kDraftUCols * 4) + h * (kSubN * 4));
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float4 t4 = urow[k];
-            z[4 * k] += t4.x; z[4 * k + 1] += t4.y; z[4 * k + 2] += t4.z; z[4 * k + 3] += t4.w;
-          }
-          // the stage is refilled by TMA (async proxy) once released: order these
-          // generic-proxy reads before that write
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_uempty + 8 * su);
 
-          // z = bias + U of 32 columns; columns past V only in the last tile
-          const int ti = tile_of(step, i, ntile);  // this tile's place in the chunk
-          const int v0 = (t_begin + ti) * kTileN + h * kSubN;
-          const int ncol = min(kSubN, p.V - v0);
-          if (ncol < kSubN) {
+          // z = bias + U of 32 columns of each tile; columns past V only in the
+          // last tile, and none at all for a missing second tile
+          const int ti0 = tile_of(step, i0, ntile);
+          const int ti1 = two ? tile_of(step, i0 + 1, ntile) : ti0;
+          const int v00 = (t_begin + ti0) * kTileN + h * kSubN;
+          const int v01 = (t_begin + ti1) * kTileN + h * kSubN;
+          const int ncol0 = min(kSubN, p.V - v00);
+          const int ncol1 = two ? min(kSubN, p.V - v01) : 0;
+          if (ncol0 < kSubN) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) z[k] = k < ncol ? z[k] : -INFINITY;
+            for (int k = 0; k < 32; ++k) z0[k] = k < ncol0 ? z0[k] : -INFINITY;
           }
-          const size_t fidx = static_cast<size_t>(2 * (t_begin + ti) + h) * p.R_pad + r;
-          if constexpr (kGreedy) {
-            int k;
-            const float mx = tree_argmax32(z, &k);
-            const int ix = v0 + k;
-            if (valid) p.fine[fidx] = make_float2(mx, __int_as_float(ix));
-            if (mx > runM || (mx == runM && ix < runIdx)) { runM = mx; runIdx = ix; }
-          } else {
-            // y = z * log2(e)/T; partial (max y, sum exp2(y - max y))
-            const float mz = tree_max32(z);
-            float mx = -INFINITY, sm = 0.f;
-            if (mz > -INFINITY) {
-              mx = mz * p.scale;
+          if (ncol1 < kSubN) {
 #pragma unroll
-              for (int k = 0; k < 32; ++k) z[k] = ex2(fmaf(z[k], p.scale, -mx));
-              sm = tree_sum32(z);
+            for (int k = 0; k < 32; ++k) z1[k] = k < ncol1 ? z1[k] : -INFINITY;
+          }
+          const size_t f0 = static_cast<size_t>(2 * (t_begin + ti0) + h) * p.R_pad + r;
+          const size_t f1 = static_cast<size_t>(2 * (t_begin + ti1) + h) * p.R_pad + r;
+          if constexpr (kGreedy) {
+            int k0, k1;
+            const float mx0 = tree_argmax32(z0, &k0);
+            const float mx1 = tree_argmax32(z1, &k1);
+            const int ix0 = v00 + k0, ix1 = v01 + k1;
+            if (valid) p.fine[f0] = make_float2(mx0, __int_as_float(ix0));
+            if (valid && two) p.fine[f1] = make_float2(mx1, __int_as_float(ix1));
+            if (mx0 > runM || (mx0 == runM && ix0 < runIdx)) { runM = mx0; runIdx = ix0; }
+            if (two && (mx1 > runM || (mx1 == runM && ix1 < runIdx))) { runM = mx1; runIdx = ix1; }
+          } else {
+            // y = z * log2(e)/T; partial (max y, sum exp2(y - max y)); an
+            // all-empty sub-tile gives (-inf, 0)
+            const float mz0 = tree_max32(z0), mz1 = tree_max32(z1);
+            const float mx0 = mz0 * p.scale, mx1 = mz1 * p.scale;
+            const float o0 = mz0 > -INFINITY ? mx0 : 0.f, o1 = mz1 > -INFINITY ? mx1 : 0.f;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              z0[k] = ex2(fmaf(z0[k], p.scale, -o0));
+              z1[k] = ex2(fmaf(z1[k], p.scale, -o1));
             }
-            if (valid) p.fine[fidx] = make_float2(mx, sm);
-            if (mx > -INFINITY) {
-              if (mx > runM) {
-                runS = (runM > -INFINITY ? runS * ex2(runM - mx) : 0.f) + sm;
-                runM = mx;
-              } else {
-                runS += sm * ex2(mx - runM);
-              }
-            }
+            const float sm0 = tree_sum32(z0), sm1 = tree_sum32(z1);
+            if (valid) p.fine[f0] = make_float2(mx0, sm0);
+            if (valid && two) p.fine[f1] = make_float2(mx1, sm1);
+            merge_partial(mx0, sm0, runM, runS);
+            merge_partial(mx1, sm1, runM, runS);
           }
         }
       }
@@ -893,7 +1003,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc(tmem_base, kDraftTmemCols);
   }
 }
 
@@ -919,6 +1029,21 @@ int encode_w2_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(rank)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 2};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), static_cast<cuuint32_t>(rank)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult rc = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W2), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+// W2 [rank, V] bf16, box 64 x 64 with 128-byte swizzle: one K-chunk of one
+// tile of the draft's W2 ring (the MN-major SW128 operand layout of the UMMA).
+static int encode_w2_kchunk_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank) {
+  auto fn = get_encode_fn();
+  if (!fn) return DSPARK_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(rank)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), static_cast<cuuint32_t>(kDraftKChunk)};
   cuuint32_t estr[2] = {1, 1};
   const CUresult rc = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W2), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -993,7 +1118,7 @@ int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
     return DSPARK_ERR_UNSUPPORTED_SHAPE;
 
   CUtensorMap tm_w2, tm_u, tm_slab;
-  if (encode_w2_map(&tm_w2, W2, V, rank) != DSPARK_OK || encode_u_map(&tm_u, U, R, gamma, V) != DSPARK_OK ||
+  if (encode_w2_kchunk_map(&tm_w2, W2, V, rank) != DSPARK_OK || encode_u_map(&tm_u, U, R, gamma, V) != DSPARK_OK ||
       encode_w2_slab_map(&tm_slab, W2, V, rank) != DSPARK_OK)
     return DSPARK_ERR_CUDA;
 
@@ -1010,7 +1135,7 @@ int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks * a.n_mtiles);
-  cfg.blockDim = dim3(kDraftThreads);
+  cfg.blockDim = dim3(kDraftKThreads);
   cfg.dynamicSmemBytes = plan.total;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
