@@ -145,6 +145,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// 2^x on the SFU (ex2.approx.ftz; results below 2^-126 flush to 0, which
+// changes no softmax sum at the fp32 precision the partials carry).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // generic-proxy writes to shared memory -> visible to the async proxy (tensor cores, TMA)
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -137,13 +137,6 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
-// 2^x on the SFU (ex2.approx.ftz; results below 2^-126 flush to 0, which
-// changes no softmax sum at the fp32 precision the partials carry).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // Waits until *word >= target (acquire).  Gives up after kWaitLimitNs or once
 // any CTA has raised the abort word; then raises it too and returns false.

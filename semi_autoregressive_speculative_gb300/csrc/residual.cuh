@@ -318,6 +318,19 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
     float runS = 0.f;  // running sum of w over this warp's half of the chunk
     // a warp with no live row in its lane quarter only keeps the rings moving
     const bool warp_works = __any_sync(0xffffffffu, valid);
+    // this row's 32 target values of the next tile, loaded one tile ahead
+    float tn[32];
+    auto load_t = [&](int i) {
+      const int v0 = (t_begin + i) * kTileN + h * kSubN;
+      const int ncol = min(kSubN, p.V - v0);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid && 4 * k < ncol) t4 = __ldg(reinterpret_cast<const float4*>(trow_ptr + v0) + k);
+        tn[4 * k] = t4.x; tn[4 * k + 1] = t4.y; tn[4 * k + 2] = t4.z; tn[4 * k + 3] = t4.w;
+      }
+    };
+    if (warp_works && ntile > 0) load_t(0);
     for (int i = 0; i < ntile; ++i) {
       const int s = i % kStages, acc = i & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, (i >> 1) & 1, abort_flag))) {
@@ -362,16 +375,13 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
       const size_t fidx = static_cast<size_t>(2 * (t_begin + i) + h) * p.R_pad + fcol;
       float tv[32];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (valid && 4 * k < ncol) t4 = __ldg(reinterpret_cast<const float4*>(trow_ptr + v0) + k);
-        tv[4 * k] = t4.x; tv[4 * k + 1] = t4.y; tv[4 * k + 2] = t4.z; tv[4 * k + 3] = t4.w;
-      }
+      for (int k = 0; k < 32; ++k) tv[k] = tn[k];
+      if (i + 1 < ntile) load_t(i + 1);
       float sw = 0.f;
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        const float pd = exp2f((v[k] + u[k]) * p.scale - l2zd);
-        const float pt = exp2f(tv[k] * p.scale - mt) * inv_zt;
+        const float pd = ex2((v[k] + u[k]) * p.scale - l2zd);
+        const float pt = ex2(tv[k] * p.scale - mt) * inv_zt;
         sw += (k < ncol) ? fmaxf(pt - pd, 0.f) : 0.f;
       }
       if (valid && fcol >= 0) p.fine[fidx] = make_float2(sw, 0.f);
