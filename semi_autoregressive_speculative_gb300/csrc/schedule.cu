@@ -2,7 +2,10 @@
 // section "按负载决定验证多少").  One CTA of 1024 threads, everything in
 // shared memory, no host round trip:
 //   1. keys (a descending, j ascending, r ascending) packed into 64 bits and
-//      bitonic-sorted (warp barriers for the passes inside a warp);
+//      bitonic-sorted in registers (E keys per thread): partners inside a
+//      warp by shuffles, partners in the same thread in registers, partners
+//      in other warps through a double-buffered shared array (one CTA
+//      barrier per such pass);
 //   2. a -> Q.40 fixed point and an integer inclusive scan: S_b is the same for
 //      every summation order;
 //   3. Theta(b) = (R + S_b 2^-40) * SPS[R + b] in fp64 for every b;
@@ -16,6 +19,77 @@
 namespace dspark {
 
 constexpr int kSchedThreads = 1024;
+
+// One bitonic compare-exchange seen from index i: keep the smaller key when i
+// is the lower index of an ascending pair (or the upper of a descending one).
+__device__ __forceinline__ uint64_t bitonic_keep(uint64_t x, uint64_t y, int i, int jj, int k) {
+  const bool keep_min = ((i & jj) == 0) == ((i & k) == 0);
+  return keep_min ? (x < y ? x : y) : (x < y ? y : x);
+}
+
+// A pass whose partner index is m ^ MJ in the same thread (MJ fixed at compile
+// time, so that the keys stay in registers).
+template <int E, int MJ>
+__device__ __forceinline__ void bitonic_in_thread(uint64_t (&x)[E], int t, int jj, int k) {
+#pragma unroll
+  for (int m = 0; m < E; ++m) {
+    if ((m ^ MJ) > m && (m ^ MJ) < E) {
+      const int m2 = m ^ MJ;
+      const uint64_t lo = x[m], hi = x[m2];
+      x[m] = bitonic_keep(lo, hi, t + kSchedThreads * m, jj, k);
+      x[m2] = bitonic_keep(hi, lo, t + kSchedThreads * m2, jj, k);
+    }
+  }
+}
+
+// Ascending bitonic sort of b0[0, 1024 E); b1 is scratch of the same size.
+// Thread t holds indices t + 1024 m, m < E, so a warp owns 32 consecutive
+// indices of every block of 1024: partners closer than 32 are exchanged by
+// shuffles, partners 1024 apart or more sit in the same thread, and the rest
+// go through shared memory (one CTA barrier per pass, the two buffers taking
+// turns).  On return b0 holds the sorted keys.  (Measured: 8 consecutive keys
+// per thread on fewer warps was slower; the network is latency-bound.)
+template <int E>
+__device__ void sort_keys(uint64_t* b0, uint64_t* b1) {
+  constexpr int n = kSchedThreads * E;
+  const int t = threadIdx.x;
+  uint64_t x[E];
+#pragma unroll
+  for (int m = 0; m < E; ++m) x[m] = b0[t + kSchedThreads * m];
+  __syncthreads();  // every key is read before the first exchange rewrites b0
+  int xp = 0;       // exchanges through shared memory so far (buffer parity)
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      if (jj < 32) {
+#pragma unroll
+        for (int m = 0; m < E; ++m) {
+          const uint64_t y = __shfl_xor_sync(0xffffffffu, x[m], jj);
+          x[m] = bitonic_keep(x[m], y, t + kSchedThreads * m, jj, k);
+        }
+      } else if (jj >= kSchedThreads) {
+        const int mj = jj / kSchedThreads;  // partner m ^ mj in this thread: 1, 2 or 4
+        if (mj == 1) bitonic_in_thread<E, 1>(x, t, jj, k);
+        else if (mj == 2) bitonic_in_thread<E, 2>(x, t, jj, k);
+        else bitonic_in_thread<E, 4>(x, t, jj, k);
+      } else {
+        uint64_t* buf = (xp & 1) ? b1 : b0;
+#pragma unroll
+        for (int m = 0; m < E; ++m) buf[t + kSchedThreads * m] = x[m];
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < E; ++m) {
+          const int i = t + kSchedThreads * m;
+          x[m] = bitonic_keep(x[m], buf[i ^ jj], i, jj, k);
+        }
+        ++xp;
+      }
+    }
+  }
+  __syncthreads();  // the last shared-memory exchange is read everywhere
+#pragma unroll
+  for (int m = 0; m < E; ++m) b0[t + kSchedThreads * m] = x[m];
+  __syncthreads();
+}
 
 struct SchedSmem {
   uint32_t keys, S, rid, cnt, total;
@@ -70,24 +144,16 @@ __global__ void __launch_bounds__(kSchedThreads)
   }
   for (int r = tid; r < R; r += kSchedThreads) cnt[r] = 0;
   __syncthreads();
-  // 2. bitonic sort, ascending.  Thread t handles indices t + 1024 m, so a warp
-  // owns 32 consecutive indices of every block of 1024: passes whose partner
-  // distance is below 32 stay inside the warp and need only a warp barrier;
-  // the CTA barrier follows the wider passes and each merge size.
-  for (int k = 2; k <= npow2; k <<= 1) {
-    for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int i = tid; i < npow2; i += kSchedThreads) {
-        const int ixj = i ^ jj;
-        if (ixj > i) {
-          const uint64_t x = keys[i], y = keys[ixj];
-          const bool up = (i & k) == 0;
-          if ((x > y) == up) { keys[i] = y; keys[ixj] = x; }
-        }
-      }
-      if (jj >= 32) __syncthreads(); else __syncwarp();
+  // 2. bitonic sort, ascending (npow2 = 1024 E, E <= 8: the host pads to 1024);
+  // the prefix-sum array is the exchange scratch
+  {
+    uint64_t* scratch = reinterpret_cast<uint64_t*>(S);
+    switch (npow2 / kSchedThreads) {
+      case 1: sort_keys<1>(keys, scratch); break;
+      case 2: sort_keys<2>(keys, scratch); break;
+      case 4: sort_keys<4>(keys, scratch); break;
+      default: sort_keys<8>(keys, scratch); break;
     }
-    // merges up to 32 wide never leave a warp; the next, wider one reads across warps
-    if (k >= 32) __syncthreads(); else __syncwarp();
   }
   // 3. fixed-point values and request ids in sorted order; S[0] = 0
   for (int i = tid; i < n; i += kSchedThreads) {
@@ -192,8 +258,9 @@ __global__ void __launch_bounds__(kSchedThreads)
 
 int launch_schedule(const float* a, int R, int gamma, const double* sps, int mode, int budget_K, int32_t* lens,
                     int32_t* total_b, int32_t* argmax_b, double* theta, int32_t* status, cudaStream_t stream) {
-  int npow2 = 1;
+  int npow2 = kSchedThreads;  // at least one key per thread
   while (npow2 < R * gamma) npow2 <<= 1;
+  static_assert(kMaxSchedule <= 8 * kSchedThreads, "the register sort holds at most 8 keys per thread");
   const SchedSmem plan = sched_smem_plan(npow2, R);
   if (cudaFuncSetAttribute(k3_schedule, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(sched_smem_plan(kMaxSchedule, kMaxSchedule).total)) != cudaSuccess)
