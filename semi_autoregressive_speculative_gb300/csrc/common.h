@@ -19,7 +19,7 @@ constexpr int kMaxChunks = 1024;   // upper bound on contiguous V-chunks per M-t
 constexpr int kUStride = kTileN * 4 + 16;  // bytes per bulk-copied U row (padded: conflict-free)
 constexpr int kPfTiles = 4;        // tiles per L2 prefetch group (a 256-column span per row)
 constexpr int kDraftThreads = 320; // warp 0 TMA producer, warp 1 MMA, warps 2..9 epilogue
-constexpr int kVerifyChunk = 2048; // target columns per verify statistics item (64 per lane)
+constexpr int kVerifyChunk = 1024; // target columns per verify statistics item (32 per lane)
 constexpr int kMaxGamma = 64;
 constexpr int kMaxSchedule = 8192; // R * gamma handled by the one-CTA scheduler
 constexpr int kMaxVerifyR = 32768; // verify keeps R + 1 row offsets in shared memory

@@ -4,7 +4,7 @@
 //
 //  k4_prepare       one CTA: verify-row offsets (exclusive scan of lens + 1),
 //                   clears the rejection list.
-//  k4_target_stats  one warp per (verify row, 2048-column chunk; row owners from a
+//  k4_target_stats  one warp per (verify row, 1024-column chunk; row owners from a
 //                   shared-memory copy of the row offsets): softmax
 //                   partials of T / temperature (or max / argmax), and the
 //                   target logit at the drafted token.
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(256) k4_target_stats(const VerifyArgs p) {
       float s = 0.f;
       if (mx > -INFINITY) {
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) s += exp2f(t[k] - mx);
+        for (int k = 0; k < kPer; ++k) s += ex2(t[k] - mx);
       }
       s = warp_sum(s);
       res = make_float2(mx, s);
