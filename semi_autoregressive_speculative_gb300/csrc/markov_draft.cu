@@ -4,25 +4,31 @@
 //
 // Per position j, on every CTA (one contiguous V-chunk of one 128-row M-tile):
 //   gather   each row's W1[x_{j-1}] goes into tensor memory as the UMMA A
-//            operand, once the sampler that drew x_{j-1} has published it
-//   tiles    W2 tiles (L2-resident after the first position) and U tiles
-//            (one 128-row x 64-column box per tile: 256 contiguous bytes per
-//            row, which is what lets the HBM stream run near its peak) come
-//            in through TMA rings; tcgen05.mma into fp32 accumulators in
-//            tensor memory, two tiles per instruction (below); the epilogue
-//            adds U, scales by log2(e)/T and
-//            reduces each 32-column sub-tile and the whole chunk to softmax
-//            partials (max, sum exp2) — (max, argmax) when greedy.  Logits
-//            never reach HBM.  The CTA then counts itself done on its M-tile.
-//   sample   one warp per request, once every chunk of its M-tile is done:
-//            merges the chunk partials into the row's max and normaliser,
-//            finds the chunk, then the 32-column sub-tile, where the
-//            cumulative mass first exceeds u * Z, recomputes those 32 logits
-//            on CUDA cores, picks x_j, writes x_j, p_d(x_j) and log Z_j and
-//            counts x_j as published on its M-tile.  Greedy: argmax of the
-//            partials.
-// The TMA producer warp never waits for the samplers: W2 and U do not depend
-// on the drafted tokens, so it streams the next position's tiles into the
+//            operand, once the samplers of the M-tile have published the
+//            previous tokens (a per-M-tile counter; the publishing sampler
+//            has already staged the row in gather order)
+//   tiles    W2 in 64-row K-chunks (L2-resident after the first position)
+//            and U tiles (one 128-row x 68-column box per tile: 272
+//            contiguous bytes per row, which is what lets the HBM stream run
+//            near its peak) come in through TMA rings, each fed by its own
+//            producer warp; tcgen05.mma into fp32 accumulators in tensor
+//            memory, two 64-column tiles per instruction (below); the
+//            epilogue takes a pair of tiles per iteration, adds U, scales by
+//            log2(e)/T and reduces each 32-column sub-tile and the whole
+//            chunk to softmax partials (max, sum exp2) — (max, argmax) when
+//            greedy.  Logits never reach HBM.  Each row's chunk partial is
+//            published as one tagged 64-bit entry (chunk_entry).
+//   sample   the CTA's requests (all 8 epilogue warps per request; one warp
+//            per request when greedy): the leader polls the row's chunk
+//            entries, merges them into the row's max and normaliser, finds
+//            the chunk, then the 32-column sub-tile, where the cumulative
+//            mass first exceeds u * Z, and the warps recompute those 32
+//            logits from a slab of W2 columns; the leader picks x_j, writes
+//            x_j, p_d(x_j) and log Z_j, stages W1[x_j] for the next gather
+//            and counts x_j as published on its M-tile.  Greedy: argmax of
+//            the entries.
+// The producer warps never wait for the samplers: W2 and U do not depend on
+// the drafted tokens, so they stream the next position's first tiles into the
 // rings while the samplers run.  Every wait is bounded (kWaitLimitNs); a CTA
 // that gives up raises a grid-wide abort word and DSPARK_STATUS_TIMEOUT.
 // Waits are polled by one thread per group (a CTA's gather, a sampler warp)
