@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per dspark_markov_draft call (one round's 16 positions) from the
 # ncu capture summarised in profiles/; valid only for the draft kernel sources
 # whose digest (draft_digest) is recorded with it.
-NCU_DRAFT_TRAFFIC = {"digest": "211cbed688b1", "bytes_per_call": 1.60e9 + 23.71e6}
+NCU_DRAFT_TRAFFIC = {"digest": "48734330b3f8", "bytes_per_call": 1.59e9 + 23.31e6}
 
 
 # ----------------------------------------------------------------------------- helpers
