@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per dspark_markov_draft call (one round's 16 positions) from the
 # ncu capture summarised in profiles/; valid only for the draft kernel sources
 # whose digest (draft_digest) is recorded with it.
-NCU_DRAFT_TRAFFIC = {"digest": "48734330b3f8", "bytes_per_call": 1.59e9 + 23.31e6}
+NCU_DRAFT_TRAFFIC = {"digest": "48734330b3f8", "workload": "r128_g16_v151936", "bytes_per_call": 1.59e9 + 23.31e6}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -372,7 +372,9 @@ def run_gpu(args):
     cstar_rows = int(np.minimum(lens_h + 1, g).sum()) if temp > 0 else 0
     cstar_bytes = rows_read * V * 4 + cstar_rows * V * 8 + (rk * V * 2 if cstar_rows else 0)
     digest = kernel_digest()
-    traffic = NCU_DRAFT_TRAFFIC["bytes_per_call"] if NCU_DRAFT_TRAFFIC["digest"] == draft_digest() else None
+    # the recorded DRAM bytes belong to one full call of the workload they were captured on
+    traffic = (NCU_DRAFT_TRAFFIC["bytes_per_call"]
+               if NCU_DRAFT_TRAFFIC["digest"] == draft_digest() and wl.name == NCU_DRAFT_TRAFFIC["workload"] else None)
 
     # ------------------------------------------------------------- end to end (host buffers)
     # Every step copies the round's inputs in from pinned host memory and reads
