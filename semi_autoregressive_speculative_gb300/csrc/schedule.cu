@@ -1,11 +1,9 @@
 // Hardware-aware prefix scheduler ("DSpark" §4.1-4.3; "投机解码的新做法" page,
 // section "按负载决定验证多少").  One CTA of 1024 threads, everything in
 // shared memory, no host round trip:
-//   1. keys (a descending, j ascending, r ascending) packed into 64 bits and
-//      bitonic-sorted in registers (E keys per thread): partners inside a
-//      warp by shuffles, partners in the same thread in registers, partners
-//      in other warps through a double-buffered shared array (one CTA
-//      barrier per such pass);
+//   1. keys (a descending, j ascending, r ascending) packed into 64 bits,
+//      written in (j, r) order and sorted by a stable radix sort on their
+//      upper 32 bits (four 8-bit passes);
 //   2. a -> Q.40 fixed point and an integer inclusive scan: S_b is the same for
 //      every summation order;
 //   3. Theta(b) = (R + S_b 2^-40) * SPS[R + b] in fp64 for every b;
@@ -20,79 +18,97 @@ namespace dspark {
 
 constexpr int kSchedThreads = 1024;
 
-// One bitonic compare-exchange seen from index i: keep the smaller key when i
-// is the lower index of an ascending pair (or the upper of a descending one).
-__device__ __forceinline__ uint64_t bitonic_keep(uint64_t x, uint64_t y, int i, int jj, int k) {
-  const bool keep_min = ((i & jj) == 0) == ((i & k) == 0);
-  return keep_min ? (x < y ? x : y) : (x < y ? y : x);
-}
+constexpr int kRadixDigits = 256;  // 8-bit digits, four passes over the upper 32 key bits
+constexpr int kSchedWarps = kSchedThreads / 32;
 
-// A pass whose partner index is m ^ MJ in the same thread (MJ fixed at compile
-// time, so that the keys stay in registers).
-template <int E, int MJ>
-__device__ __forceinline__ void bitonic_in_thread(uint64_t (&x)[E], int t, int jj, int k) {
-#pragma unroll
-  for (int m = 0; m < E; ++m) {
-    if ((m ^ MJ) > m && (m ^ MJ) < E) {
-      const int m2 = m ^ MJ;
-      const uint64_t lo = x[m], hi = x[m2];
-      x[m] = bitonic_keep(lo, hi, t + kSchedThreads * m, jj, k);
-      x[m2] = bitonic_keep(hi, lo, t + kSchedThreads * m2, jj, k);
-    }
-  }
-}
-
-// Ascending bitonic sort of b0[0, 1024 E); b1 is scratch of the same size.
-// Thread t holds indices t + 1024 m, m < E, so a warp owns 32 consecutive
-// indices of every block of 1024: partners closer than 32 are exchanged by
-// shuffles, partners 1024 apart or more sit in the same thread, and the rest
-// go through shared memory (one CTA barrier per pass, the two buffers taking
-// turns).  On return b0 holds the sorted keys.  (Measured: 8 consecutive keys
-// per thread on fewer warps was slower; the network is latency-bound.)
+// Stable LSD radix sort of b0[0, 1024 E) by key bits 32..63, ascending; b1 is
+// scratch of the same size and hist holds (32 + 8) x 256 ints.  Thread t =
+// 32 w + lane handles elements 32 E w + 32 m + lane, m < E (the keys stay in
+// shared memory), so that within a warp the order (slot, lane) is the element
+// order and the per-slot ranks from __match_any_sync are stable.  Per pass: each warp counts its digits
+// (hist[w][d]), the counts are scanned in (digit, warp) order, and each key
+// goes to its digit's base + the keys of that digit in earlier warps + its
+// rank in the warp.  On return b0 holds the sorted keys.
 template <int E>
-__device__ void sort_keys(uint64_t* b0, uint64_t* b1) {
-  constexpr int n = kSchedThreads * E;
-  const int t = threadIdx.x;
-  uint64_t x[E];
+__device__ void radix_sort_keys(uint64_t* b0, uint64_t* b1, int* hist) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const unsigned below = (1u << lane) - 1u;
+  int* gsum = hist + kSchedWarps * kRadixDigits;  // [4][256]: counts of warps 8g .. 8g+7
+  int* gbase = gsum + 4 * kRadixDigits;           // [4][256]: first position of (digit, warp group)
+  uint64_t* src = b0;
+  uint64_t* dst = b1;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int sh = 32 + 8 * pass;
+    for (int i = t; i < kSchedWarps * kRadixDigits; i += kSchedThreads) hist[i] = 0;
+    __syncthreads();
+    int rd[E];  // rank in the warp << 8 | digit
 #pragma unroll
-  for (int m = 0; m < E; ++m) x[m] = b0[t + kSchedThreads * m];
-  __syncthreads();  // every key is read before the first exchange rewrites b0
-  int xp = 0;       // exchanges through shared memory so far (buffer parity)
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      if (jj < 32) {
+    for (int m = 0; m < E; ++m) {
+      const int d = static_cast<int>((src[32 * E * w + 32 * m + lane] >> sh) & 0xFFu);
+      const unsigned peers = __match_any_sync(0xffffffffu, d);
+      const int before = hist[w * kRadixDigits + d];  // this digit in the warp's earlier slots
+      __syncwarp();
+      if ((peers & below) == 0) hist[w * kRadixDigits + d] = before + __popc(peers);
+      __syncwarp();
+      rd[m] = ((before + __popc(peers & below)) << 8) | d;
+    }
+    __syncthreads();
+    {  // exclusive counts over the warps of each group of 8, per digit
+      const int d = t & (kRadixDigits - 1), g = t >> 8;
+      int run = 0;
+      for (int ww = 8 * g; ww < 8 * g + 8; ++ww) {
+        const int c = hist[ww * kRadixDigits + d];
+        hist[ww * kRadixDigits + d] = run;
+        run += c;
+      }
+      gsum[g * kRadixDigits + d] = run;
+    }
+    __syncthreads();
+    if (w == 0) {  // digit bases (exclusive over digits), then each (digit, group) start
+      int tot[8];
+      int sum = 0;
 #pragma unroll
-        for (int m = 0; m < E; ++m) {
-          const uint64_t y = __shfl_xor_sync(0xffffffffu, x[m], jj);
-          x[m] = bitonic_keep(x[m], y, t + kSchedThreads * m, jj, k);
+      for (int k = 0; k < 8; ++k) {
+        const int d = 8 * lane + k;
+        tot[k] = gsum[d] + gsum[kRadixDigits + d] + gsum[2 * kRadixDigits + d] + gsum[3 * kRadixDigits + d];
+        sum += tot[k];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int base = incl - sum;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int d = 8 * lane + k;
+        int gb = base;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          gbase[g * kRadixDigits + d] = gb;
+          gb += gsum[g * kRadixDigits + d];
         }
-      } else if (jj >= kSchedThreads) {
-        const int mj = jj / kSchedThreads;  // partner m ^ mj in this thread: 1, 2 or 4
-        if (mj == 1) bitonic_in_thread<E, 1>(x, t, jj, k);
-        else if (mj == 2) bitonic_in_thread<E, 2>(x, t, jj, k);
-        else bitonic_in_thread<E, 4>(x, t, jj, k);
-      } else {
-        uint64_t* buf = (xp & 1) ? b1 : b0;
-#pragma unroll
-        for (int m = 0; m < E; ++m) buf[t + kSchedThreads * m] = x[m];
-        __syncthreads();
-#pragma unroll
-        for (int m = 0; m < E; ++m) {
-          const int i = t + kSchedThreads * m;
-          x[m] = bitonic_keep(x[m], buf[i ^ jj], i, jj, k);
-        }
-        ++xp;
+        base += tot[k];
       }
     }
-  }
-  __syncthreads();  // the last shared-memory exchange is read everywhere
+    __syncthreads();
 #pragma unroll
-  for (int m = 0; m < E; ++m) b0[t + kSchedThreads * m] = x[m];
-  __syncthreads();
+    for (int m = 0; m < E; ++m) {
+      const int d = rd[m] & 0xFF;
+      dst[gbase[(w >> 3) * kRadixDigits + d] + hist[w * kRadixDigits + d] + (rd[m] >> 8)] =
+          src[32 * E * w + 32 * m + lane];
+    }
+    __syncthreads();
+    uint64_t* const tmp = src;
+    src = dst;
+    dst = tmp;
+  }
+  // four passes: the last one wrote b0
 }
 
 struct SchedSmem {
-  uint32_t keys, S, rid, cnt, total;
+  uint32_t keys, S, rid, cnt, hist, total;
 };
 __host__ __device__ inline SchedSmem sched_smem_plan(int npow2, int R) {
   SchedSmem s;
@@ -103,6 +119,7 @@ __host__ __device__ inline SchedSmem sched_smem_plan(int npow2, int R) {
   off = (off + 15u) & ~15u;
   s.cnt = off;  off += 4u * R;             // per-request admitted counts
   off = (off + 15u) & ~15u;
+  s.hist = off; off += 4u * (kSchedWarps + 8) * kRadixDigits;  // radix counts and bases
   s.total = off + 64;                      // + reduction scratch
   return s;
 }
@@ -117,6 +134,7 @@ __global__ void __launch_bounds__(kSchedThreads)
   int64_t* S = reinterpret_cast<int64_t*>(sm + plan.S);
   uint16_t* rid = reinterpret_cast<uint16_t*>(sm + plan.rid);
   int32_t* cnt = reinterpret_cast<int32_t*>(sm + plan.cnt);
+  int* hist = reinterpret_cast<int*>(sm + plan.hist);
   double* th = reinterpret_cast<double*>(sm + plan.keys);
   __shared__ int s_red_b[32];
   __shared__ unsigned long long s_red_t[32];
@@ -139,20 +157,24 @@ __global__ void __launch_bounds__(kSchedThreads)
       const int r = i / gamma, j = i - r * gamma;
       key = (static_cast<uint64_t>(0xFFFFFFFFu - bits) << 32) | (static_cast<uint64_t>(j) << 16) |
             static_cast<uint64_t>(r);
+      // stored in (j, r) order: the low key bits ascending, so that a stable
+      // sort by the upper 32 bits is the full 64-bit order
+      keys[j * R + r] = key;
+    } else {
+      keys[i] = key;
     }
-    keys[i] = key;
   }
   for (int r = tid; r < R; r += kSchedThreads) cnt[r] = 0;
   __syncthreads();
-  // 2. bitonic sort, ascending (npow2 = 1024 E, E <= 8: the host pads to 1024);
-  // the prefix-sum array is the exchange scratch
+  // 2. stable radix sort by a, ascending key (npow2 = 1024 E, E <= 8: the host
+  // pads to 1024); the prefix-sum array is the scratch buffer
   {
     uint64_t* scratch = reinterpret_cast<uint64_t*>(S);
     switch (npow2 / kSchedThreads) {
-      case 1: sort_keys<1>(keys, scratch); break;
-      case 2: sort_keys<2>(keys, scratch); break;
-      case 4: sort_keys<4>(keys, scratch); break;
-      default: sort_keys<8>(keys, scratch); break;
+      case 1: radix_sort_keys<1>(keys, scratch, hist); break;
+      case 2: radix_sort_keys<2>(keys, scratch, hist); break;
+      case 4: radix_sort_keys<4>(keys, scratch, hist); break;
+      default: radix_sort_keys<8>(keys, scratch, hist); break;
     }
   }
   // 3. fixed-point values and request ids in sorted order; S[0] = 0
