@@ -70,6 +70,16 @@ size_t dspark_workspace_size(int R, int gamma, int V, int rank, int d);
 /* Enqueue a zeroing of the workspace status word. */
 int dspark_clear_status(void *workspace, void *stream);
 
+/* Self-test of the device-side timeout path.  Enqueues one kernel in which a
+ * thread waits, through the same bounded mbarrier wait the pipelined kernels
+ * use on their rings, for a phase that nothing ever completes.  When the wait
+ * gives up (after 2 s) the kernel ORs DSPARK_STATUS_TIMEOUT into the
+ * workspace status word and returns; nothing faults, and the context stays
+ * usable.  workspace: any 256-byte-aligned device buffer whose first int32 is
+ * the status word.  Returns DSPARK_ERR_INVALID_ARG for a null or misaligned
+ * workspace, DSPARK_ERR_CUDA if the launch fails. */
+int dspark_selftest_bounded_wait(void *workspace, void *stream);
+
 /*
  * Markov-head sequential draft ("DSpark" §2.2 eq. p_k and §2.3; the loop of
  * §6.2).  For each request r and position j = 0..gamma-1, with x_{-1} = anchor:

@@ -26,7 +26,7 @@ DSPARK_STATUS_BAD_LENGTH = 8
 MODE_EARLY_STOP, MODE_TOP_K, MODE_FIXED = 0, 1, 2
 
 EXPORTS = ("dspark_workspace_size", "dspark_clear_status", "dspark_markov_draft", "dspark_confidence",
-           "dspark_schedule", "dspark_verify", "dspark_markov_draft_noalloc")
+           "dspark_schedule", "dspark_verify", "dspark_markov_draft_noalloc", "dspark_selftest_bounded_wait")
 
 _lib = None
 
@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
         L.dspark_workspace_size.argtypes = [I, I, I, I, I]
         L.dspark_clear_status.restype = I
         L.dspark_clear_status.argtypes = [P, P]
+        L.dspark_selftest_bounded_wait.restype = I
+        L.dspark_selftest_bounded_wait.argtypes = [P, P]
         L.dspark_markov_draft.restype = I
         L.dspark_markov_draft.argtypes = [P, P, P, P, I, I, I, I, F, U64, U32, P, P, P, P, SZ, P]
         L.dspark_confidence.restype = I
@@ -99,6 +101,12 @@ def dspark_workspace_size(R: int, gamma: int, V: int, rank: int, d: int) -> int:
 
 def dspark_clear_status(workspace, stream=None) -> None:
     _check("dspark_clear_status", lib().dspark_clear_status(_ptr(workspace), _stream(stream)))
+
+
+def dspark_selftest_bounded_wait(workspace, stream=None) -> None:
+    """Enqueue the timeout self-test: a bounded device wait that gives up and
+    sets DSPARK_STATUS_TIMEOUT in the workspace status word (about 2 s)."""
+    _check("dspark_selftest_bounded_wait", lib().dspark_selftest_bounded_wait(_ptr(workspace), _stream(stream)))
 
 
 def read_status(workspace) -> int:

@@ -147,6 +147,22 @@ def test_nonfinite_logits_reported():
     assert tok.min() >= 0 and tok.max() < wl.V
 
 
+def test_bounded_wait_gives_up_and_reports_timeout():
+    # a device wait on a phase that nothing completes gives up after its limit,
+    # reports DSPARK_STATUS_TIMEOUT and returns: the context stays usable
+    from semi_autoregressive_speculative_gb300 import DSPARK_STATUS_TIMEOUT, dspark_selftest_bounded_wait
+    wl = synth.scaled(synth.WORKLOADS["tiny_r4_g7_v4096"], R=4, gamma=3, V=512, d=16, name="timeout")
+    dr, inp = device_round(wl)
+    dspark_selftest_bounded_wait(dr.workspace)
+    torch.cuda.synchronize()
+    assert dr.status() & DSPARK_STATUS_TIMEOUT
+    dr.clear_status()
+    dr.draft(1.0, wl.seed, 0)
+    tok = host(dr.tokens)
+    assert tok.min() >= 0 and tok.max() < wl.V
+    assert dr.status() == 0
+
+
 def test_one_graph_many_rounds_device_decided_lengths():
     # One captured round replayed on new inputs: the scheduler decides each
     # request's verify length on the device, and verify consumes those
