@@ -22,6 +22,7 @@ import glob
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -41,15 +42,29 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per dspark_markov_draft call (one round's 16 positions) from the
 # ncu capture summarised in profiles/; valid only for the draft kernel sources
 # whose digest (draft_digest) is recorded with it.
-NCU_DRAFT_TRAFFIC = {"digest": "48734330b3f8", "workload": "r128_g16_v151936", "bytes_per_call": 1.59e9 + 23.31e6}
+NCU_DRAFT_TRAFFIC = {"digest": "a28fc0263521", "workload": "r128_g16_v151936", "bytes_per_call": 1600726016 + 23566592}
 
 
 # ----------------------------------------------------------------------------- helpers
-def _digest(paths) -> str:
+_C_TOKENS = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'', re.S)
+
+
+def code_text(src: str) -> str:
+    """C/C++/CUDA source as the compiler sees it, up to layout: comments
+    dropped (string and character literals kept), whitespace runs collapsed.
+    Editing a comment or re-wrapping lines leaves it unchanged."""
+    out = _C_TOKENS.sub(lambda m: " " if m.group(0)[0] == "/" else m.group(0), src)
+    return " ".join(out.split())
+
+
+def _digest(paths, code_only: bool = False) -> str:
     h = hashlib.sha1()
     for f in sorted(paths):
         with open(f, "rb") as fh:
-            h.update(fh.read())
+            data = fh.read()
+        if code_only:
+            data = code_text(data.decode("utf-8")).encode("utf-8")
+        h.update(os.path.basename(f).encode() + b"\0" + data)
     return h.hexdigest()[:12]
 
 
@@ -59,10 +74,12 @@ def kernel_digest() -> str:
 
 
 def draft_digest() -> str:
-    """Digest of the sources the draft kernel is compiled from."""
+    """Digest of the code (comments and layout aside) of the sources the draft
+    kernel is compiled from."""
     csrc = os.path.join(ROOT, "semi_autoregressive_speculative_gb300", "csrc")
     names = ["markov_draft.cu", "common.h", "device.cuh", "search.cuh", "vocab_common.h"]
-    return _digest([os.path.join(csrc, n) for n in names] + [os.path.join(ROOT, "include", "dspark.h")])
+    return _digest([os.path.join(csrc, n) for n in names] + [os.path.join(ROOT, "include", "dspark.h")],
+                   code_only=True)
 
 
 def measured_peaks():

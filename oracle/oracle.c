@@ -14,7 +14,7 @@
  *              (anrans.github.io ai-infra-handbooks, serving/frontier/spec-next)
  *   [Summary]  "DSpark: Speculative decodingを活用したLLM推論の高速化" (ja.news.hada.io)
  *
- * Readings where the pages are silent (each is also listed in the design doc):
+ * Readings where the pages are silent:
  *   - temperature T divides the combined logits (U + bias) for draft and target
  *     alike; T == 0 means greedy argmax with the lowest index winning ties;
  *   - greedy decisions are taken on fp32 logits (the kernel's precision): the

@@ -75,6 +75,14 @@ def test_draft_full_size_sampled(name):
         tok, pd, lz = host(dr.tokens), host(dr.pd), host(dr.logZ)
         assert tok.min() >= 0 and tok.max() < wl.V
         assert np.all(pd > 0) and np.all(pd <= 1.0 + 1e-6) and np.all(np.isfinite(lz))
-        div, ties = check_draft(wl, inp, tok, pd, lz, temp, 0, sample_requests(wl.R))
-        assert div <= 1 and ties == 0
+        # greedy: every request (tokens are bit-exact); sampled: three rows of
+        # every lane quarter of every M-tile
+        rows = range(wl.R) if temp == 0.0 else sample_requests(wl.R)
+        counts = {}
+        div, ties = check_draft(wl, inp, tok, pd, lz, temp, 0, rows, counts)
+        assert ties == 0
+        # each divergence was checked to lie within the CDF tolerance; after
+        # one, a request's later positions are not compared, so require that
+        # most draws were compared
+        assert counts["compared"] >= 0.5 * len(rows) * wl.gamma, (div, counts)
     assert dr.status() == 0

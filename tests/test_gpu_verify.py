@@ -4,8 +4,11 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import check_verify, device_round, host, sample_requests, verify_inputs
+import oracle
+from gpu_helpers import (check_verify, device_round, host, oracle_confidence, oracle_draft, sample_requests,
+                         verify_inputs, weights)
 from semi_autoregressive_speculative_gb300 import synth
+from semi_autoregressive_speculative_gb300.round import MODE_EARLY_STOP, MODE_TOP_K
 
 pytestmark = pytest.mark.gpu
 
@@ -54,8 +57,49 @@ def test_verify_many_rows_two_mtiles():
 def test_verify_full_size_sampled(name):
     wl = synth.WORKLOADS[name]
     for temperature in wl.temperatures:
-        na, nx, ex = _run(wl, temperature, sample_requests(wl.R))
-        assert ex <= 1
+        rows = sample_requests(wl.R)
+        na, nx, ex = _run(wl, temperature, rows)
+        assert ex <= max(1, len(rows) // 4)  # each exemption checked within tolerance
+
+
+def test_verify_full_size_staircase_every_request():
+    # The scheduler/verify stress workload at full size (R = 512: four
+    # M-tiles; V = 32768; target noise std 0.3 on the first half of the
+    # requests, 2 on the second), every request compared with the oracle.
+    # Draft, confidence and both schedules come from the oracle on all
+    # requests, so that verify sees the ragged lengths its early-stop and
+    # Top-K schedules produce on the staircase SPS table.  Here the early stop
+    # lands just below the first cliff (B = 1024, b = 511); the Top-K budget,
+    # the one a round kept from two rounds earlier, is taken as 3 R = 1536, a
+    # budget past that cliff.
+    wl = synth.WORKLOADS["r512_g16_v32768_staircase"]
+    temperature, rnd = wl.temperatures[0], 0
+    dr, inp = device_round(wl)
+    W1, W2, w = weights(wl)
+    every = np.arange(wl.R)
+    drafted = oracle_draft(inp.U, W1, W2, inp.anchors, temperature, wl.seed, rnd, every)
+    _, a = oracle_confidence(inp.h, W1, w, inp.anchors, drafted[0])
+    sps = synth.sps_table(wl)
+    early = oracle.schedule(a, sps, MODE_EARLY_STOP)
+    topk = oracle.schedule(a, sps, MODE_TOP_K, 3 * wl.R)
+    tokens, pd, lz, T, _ = verify_inputs(wl, inp, rnd, every, temperature, drafted=drafted)
+    dr.T.copy_(torch.from_numpy(T))
+    dr.tokens.copy_(torch.from_numpy(tokens))
+    dr.pd.copy_(torch.from_numpy(pd))
+    dr.logZ.copy_(torch.from_numpy(lz))
+    seen = []
+    for sched in (early, topk):
+        lens = sched["lens"].astype(np.int32)
+        assert 0 < lens.sum() < wl.R * wl.gamma and lens.min() < lens.max()  # ragged
+        seen.append(tuple(lens))
+        dr.lens.copy_(torch.from_numpy(lens))
+        dr.verify(temperature, wl.seed, rnd)
+        na, nx = host(dr.n_accept), host(dr.next_token)
+        assert np.all(na >= 0) and np.all(na <= lens)
+        ex = check_verify(wl, inp, T, tokens, lens, na, nx, temperature, rnd, every)
+        assert ex <= wl.R // 8  # each exemption checked within tolerance
+        assert dr.status() == 0
+    assert seen[0] != seen[1]
 
 
 def _run_c_star(wl, temperature, compare, lens=None, rnd=0):
@@ -117,5 +161,6 @@ def test_c_star_many_mtiles():
 
 def test_c_star_full_size():
     wl = synth.WORKLOADS["r128_g16_v151936"]
-    _, ex = _run_c_star(wl, 1.0, sample_requests(wl.R))
-    assert ex <= 1
+    rows = sample_requests(wl.R)
+    _, ex = _run_c_star(wl, 1.0, rows)
+    assert ex <= max(1, len(rows) // 4)
