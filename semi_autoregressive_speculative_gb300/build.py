@@ -1,10 +1,13 @@
 """Build libdspark.so in-tree with nvcc for sm_103a (no GPU needed).
 
-    python -m semi_autoregressive_speculative_gb300.build [--force]
+    python -m semi_autoregressive_speculative_gb300.build [--force] [--trace]
 
 Each translation unit compiles in parallel; the objects link into
 ``semi_autoregressive_speculative_gb300/lib/libdspark.so`` with a static CUDA
 runtime, so the library loads on any host with the NVIDIA driver.
+``--trace`` builds ``lib/libdspark_trace.so`` instead: the same sources with
+the draft kernel's phase stamps compiled in (-DDSPARK_DRAFT_TRACE), for the
+``draft_trace`` tool; the product library never carries them.
 """
 from __future__ import annotations
 
@@ -36,24 +39,30 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+TRACE_LIB = os.path.join(LIBDIR, "libdspark_trace.so")
+
+
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    lib = TRACE_LIB if trace else LIB
+    objdir = os.path.join(OBJDIR, "trace") if trace else OBJDIR
+    defines = ["-DDSPARK_DRAFT_TRACE"] if trace else []
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(objdir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     procs = []
     objs = []
     for src in _sources():
-        obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
-        cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        cmd = [NVCC, *ARCH, *FLAGS, *defines, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
@@ -66,15 +75,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(os.path.basename(f) for f in failed))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.run([NVCC, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
+    ap.add_argument("--trace", action="store_true", help="build lib/libdspark_trace.so (draft phase stamps)")
     args = ap.parse_args()
-    print(build(force=args.force, verbose=args.verbose))
+    print(build(force=args.force, verbose=args.verbose, trace=args.trace))

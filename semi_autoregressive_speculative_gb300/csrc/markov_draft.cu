@@ -37,6 +37,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstring>
 #include <mutex>
 #include <utility>
 
@@ -63,19 +64,59 @@ constexpr int kDraftAccPairs = 3;    // fp32 accumulator pairs (2 x 64 columns e
 constexpr int kDraftACol = kDraftAccPairs * 2 * kTileN;  // first tensor-memory column of the A operand
 constexpr int kDraftTmemCols = 512;                      // accumulators + A (rank / 2 <= 128 columns)
 static_assert(kDraftACol + 128 <= kDraftTmemCols, "tensor-memory plan");
-// warp 0 W2 producer, warp 1 MMA issuer, warps 2..9 epilogue and samplers, warp 10 U producer
-constexpr int kDraftKThreads = kDraftThreads + 32;
+// warp 0 W2 producer, warp 1 MMA issuer, warps 2..9 epilogue and samplers,
+// warp 10 U producer, warp 11 U copier
+constexpr int kDraftKThreads = kDraftThreads + 64;
 constexpr int kUWarp = 10;
-// A U tile is one 128-row x 68-column box: the 64 columns of the tile plus the
-// first 4 of the next.  Each request row is one 272-byte run in HBM (runs of
-// 256 bytes and more keep the stream near the copy rate; 128-byte runs lose
-// about a third of it), and the 272-byte row pitch in shared memory puts 8
-// consecutive rows on 8 different bank groups, so the epilogue's 16-byte reads
-// are conflict-free.
-constexpr int kDraftUCols = kTileN + 4;
-constexpr int kDraftUBytes = kMTile * kDraftUCols * 4;
+constexpr int kCopyWarp = 11;
+// U never passes through registers: each 128-row x 64-column U tile lands in
+// shared memory by TMA in the 128-byte-swizzled K-major layout and is copied
+// into its accumulator pair in tensor memory (tcgen05.cp, by the copier warp)
+// before the MMA, which then accumulates the Markov bias on top of it.  The
+// copier runs as far ahead as the accumulator slots allow: while the samplers
+// of a position run, the next position's first three pairs are already in
+// tensor memory and the ring refills behind them, so the HBM stream no longer
+// stops between positions.
+//   fast layout (R % 8 == 0, a whole tile): one 5-D TMA box {32 columns,
+//     8 rows, 2 halves, 16 row groups} per tile, so that each request row's
+//     256 contiguous bytes are fetched together (a box per 32-column half
+//     streams at about 70 % of that rate).  Row group g holds half h of its
+//     8 rows at byte g * 2048 + h * 1024 (SBO 2048).
+//   general layout (a ragged last tile, or R % 8 != 0): two 3-D boxes
+//     {32, 1, 128} per tile, columns past V and rows past R zero-filled; half
+//     h at byte h * 16384, rows at 128 bytes (SBO 1024).
+constexpr int kDraftUBytes = kMTile * kTileN * 4;  // one U tile (32 KB, 1024-aligned stages)
 constexpr int kEpiThreads = kDraftThreads - 64;  // warps 2..9
 constexpr int kMaxDraftV = 1 << 24;               // vocabulary bound of the 32-bit chunk arithmetic
+
+// Phase tracing (compiled only with -DDSPARK_DRAFT_TRACE, into a separate
+// build of the library used by the draft_trace tool; the product build has
+// none of it).  Every CTA stamps the global timer (ns) at each event of each
+// position into trace[(position * n_ctas + cta) * kTraceEvents + event].
+enum TraceEvent {
+  kEvAReady = 0,      // the position's A operand is in tensor memory (gather done)
+  kEvFirstAcc = 1,    // the first accumulator pair of the position is ready
+  kEvTilesDone = 2,   // the CTA's last tile pair of the position is reduced
+  kEvEntry = 3,       // the CTA's chunk entries are published
+  kEvPollDone = 4,    // sampler (the CTA's first request): every chunk entry seen
+  kEvSlabIssued = 5,  // sampler: crossing sub-tile found, slab copy issued
+  kEvSlabLanded = 6,  // sampler: slab in shared memory
+  kEvPicked = 7,      // sampler: token picked
+  kEvPublished = 8,   // sampler: token published (W1 row staged, counted)
+  kEvReadySeen = 9,   // the previous position's tokens of the M-tile are all published
+  kTraceEvents = 10
+};
+#ifdef DSPARK_DRAFT_TRACE
+#define DRAFT_TRACE(p, step, ev)                                                                         \
+  do {                                                                                                   \
+    if ((p).trace)                                                                                       \
+      (p).trace[(static_cast<size_t>(step) * gridDim.x + blockIdx.x) * kTraceEvents + (ev)] = global_ns(); \
+  } while (0)
+#else
+#define DRAFT_TRACE(p, step, ev) \
+  do {                           \
+  } while (0)
+#endif
 
 struct DraftArgs {
   const float* U;          // [R, gamma, V]
@@ -86,11 +127,14 @@ struct DraftArgs {
   float* pd_tok;           // [R, gamma]
   float* logZ;             // [R, gamma]
   unsigned long long* centry;  // [R_pad][n_chunks] tagged chunk entries (see chunk_entry)
-  float2* fine;            // [2 * n_tiles][R_pad]
+  unsigned long long* fine;  // [2 * n_tiles][R_pad] tagged sub-tile partials (sampled draws only; see fine_word)
   int32_t* status;
   uint32_t* ready;         // [n_mtiles] tokens published, 16 words apart
   uint32_t* abort;         // any CTA gave up on a wait
   uint4* abuf;             // each row's next A operand (W1 row of its last token), gather-ordered
+#ifdef DSPARK_DRAFT_TRACE
+  unsigned long long* trace;  // [gamma][n_ctas][kTraceEvents] or null
+#endif
   int R, R_pad, gamma, V, rank, n_tiles, n_chunks, n_mtiles;
   float scale;             // log2(e) / T (1 when greedy)
   uint64_t seed;
@@ -101,7 +145,7 @@ struct DraftArgs {
 // (w0 + s * wstride), never by indexing an array with the stage number: a
 // runtime-indexed array would put the whole plan in local memory.
 struct DraftSmem {
-  uint32_t w0, wstride, u0, half, bars, slots, part, wts, ev, slab, total;
+  uint32_t w0, wstride, u0, half, bars, slots, part, wts, ev, slab, total;  // u0 and w0 1024-aligned
   __host__ __device__ uint32_t w(int s) const { return w0 + static_cast<uint32_t>(s) * wstride; }
   __host__ __device__ uint32_t u(int s) const { return u0 + static_cast<uint32_t>(s) * kDraftUBytes; }
 };
@@ -127,13 +171,16 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+// Relaxed (single-copy atomic, unordered) 64-bit accesses: the chunk entries
+// and the sub-tile partials carry their position tag in the word itself, so a
+// reader needs no ordering against other writes, only a tag that matches.
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
   unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
   uint32_t v;
@@ -288,13 +335,35 @@ __device__ __forceinline__ void publish_token(const DraftArgs& p, int r, int ste
   }
 }
 
-// A chunk's partial for one row, published by its CTA in one 64-bit release
+// A 32-column sub-tile partial of one row, as one 64-bit word written with a
+// relaxed store: the low word is the sub-tile's reference o (its maximum y in
+// the log2 domain, with the low kFineTagBits mantissa bits replaced by the
+// position tag), the high word is sum over the columns of 2^(y - o).  (o, sum)
+// states the sub-tile's mass exactly as (max, sum) would: o moves the
+// reference by at most 2^-16 relative, and the sum is taken against o itself.
+// An empty sub-tile (columns past V only) has o = -FLT_MAX (tagged) and sum 0.
+// The words are zeroed at the start of every call, so only this call's
+// position can match a tag.
+constexpr uint32_t kFineTagBits = 7;  // tags 1..kMaxGamma
+constexpr uint32_t kFineTagMask = (1u << kFineTagBits) - 1u;
+static_assert(kMaxGamma <= static_cast<int>(kFineTagMask), "position tags");
+__device__ __forceinline__ float fine_ref(float ymax, uint32_t tag) {
+  const float o = ymax > -INFINITY ? ymax : -3.4028234663852886e38f;
+  return __uint_as_float((__float_as_uint(o) & ~kFineTagMask) | tag);
+}
+__device__ __forceinline__ unsigned long long fine_word(float o, float sum) {
+  return (static_cast<unsigned long long>(__float_as_uint(sum)) << 32) | __float_as_uint(o);
+}
+
+// A chunk's partial for one row, published by its CTA in one 64-bit relaxed
 // store: the low word is a float (sampled: the chunk's log2-sum-exp2
 // L = max + log2(sum), greedy: its maximum), the high word carries the
 // position tag (position + 1) in its top 8 bits and, greedy, the argmax in its
 // low 24 bits.  The samplers poll their row's entries directly: no CTA count,
 // and each chunk is folded in as soon as it lands.  Entries are zeroed at the
-// start of every call, so a tag from an earlier call never matches.
+// start of every call, so a tag from an earlier call never matches.  No data
+// is ordered behind an entry (the sub-tile partials carry their own tags), so
+// it needs no release and its readers no acquire.
 __device__ __forceinline__ unsigned long long chunk_entry(float lo, uint32_t tag, uint32_t idx) {
   return (static_cast<unsigned long long>((tag << 24) | idx) << 32) | __float_as_uint(lo);
 }
@@ -302,9 +371,10 @@ __device__ __forceinline__ unsigned long long chunk_entry(float lo, uint32_t tag
 constexpr int kEntriesPerLane = kMaxSampleChunks / 32;
 
 // One warp waits until every chunk entry of row r carries `tag`; lane l gets
-// the entries of chunks k * 32 + l in e[k] (0 past n_chunks).  Polls with an
-// acquire load per pending entry and a short sleep; gives up (false, the same
-// in every lane, abort word raised) after kWaitLimitNs or on abort.
+// the entries of chunks k * 32 + l in e[k] (0 past n_chunks).  Polls with a
+// relaxed load per pending entry (all in flight together) and a short sleep;
+// gives up (false, the same in every lane, abort word raised) after
+// kWaitLimitNs or on abort.
 __device__ __forceinline__ bool poll_row(const DraftArgs& p, int r, uint32_t tag,
                                          unsigned long long (&e)[kEntriesPerLane]) {
   const int lane = threadIdx.x & 31;
@@ -320,7 +390,7 @@ __device__ __forceinline__ bool poll_row(const DraftArgs& p, int r, uint32_t tag
 #pragma unroll
     for (int k = 0; k < kEntriesPerLane; ++k) {
       if (pending & (1u << k)) {
-        const unsigned long long v = ld_acquire_gpu_u64(row + k * 32 + lane);
+        const unsigned long long v = ld_relaxed_gpu_u64(row + k * 32 + lane);
         if (static_cast<uint32_t>(v >> 56) == tag) {
           e[k] = v;
           pending &= ~(1u << k);
@@ -338,8 +408,46 @@ __device__ __forceinline__ bool poll_row(const DraftArgs& p, int r, uint32_t tag
     }
     __nanosleep(32);
   }
-  __syncwarp();  // every lane's later loads are ordered after all the acquires
+  __syncwarp();
   return true;
+}
+
+// One warp loads the sub-tile partials [tb2, tb2 + nsub) of row r (lane l
+// gets sub-tile k * 32 + l in fw[k], 0 past nsub), re-reading any whose tag
+// is not yet `tag` (a partial written before its chunk entry may still be in
+// flight).  False (the same in every lane, abort word raised) after
+// kWaitLimitNs or on abort.
+__device__ __forceinline__ bool load_fine(const DraftArgs& p, int r, int tb2, int nsub, uint32_t tag,
+                                          unsigned long long (&fw)[kEntriesPerLane]) {
+  const int lane = threadIdx.x & 31;
+  uint32_t pending = 0;
+#pragma unroll
+  for (int k = 0; k < kEntriesPerLane; ++k) {
+    fw[k] = 0ull;
+    if (k * 32 + lane < nsub) pending |= 1u << k;
+  }
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+#pragma unroll
+    for (int k = 0; k < kEntriesPerLane; ++k) {
+      if (pending & (1u << k)) {
+        const unsigned long long v = ld_relaxed_gpu_u64(p.fine + static_cast<size_t>(tb2 + k * 32 + lane) * p.R_pad + r);
+        if ((static_cast<uint32_t>(v) & kFineTagMask) == tag) {
+          fw[k] = v;
+          pending &= ~(1u << k);
+        }
+      }
+    }
+    if (__all_sync(0xffffffffu, pending == 0)) return true;
+    if ((it & 15u) == 15u) {
+      int bad = 0;
+      if (lane == 0) bad = ld_relaxed_gpu(p.abort) != 0 || global_ns() - t0 > kWaitLimitNs;
+      if (__shfl_sync(0xffffffffu, bad, 0)) {
+        if (lane == 0) atomicExch(p.abort, 1u);
+        return false;
+      }
+    }
+  }
 }
 
 // Greedy sampler for request r (one warp): waits for every chunk entry of the
@@ -351,6 +459,7 @@ __device__ __forceinline__ bool sample_greedy(const DraftArgs& p, int r, int ste
   const size_t out = static_cast<size_t>(r) * p.gamma + step;
   unsigned long long ent[kEntriesPerLane];
   if (!poll_row(p, r, static_cast<uint32_t>(step + 1), ent)) return false;
+  if (lane == 0 && r == static_cast<int>(blockIdx.x)) DRAFT_TRACE(p, step, kEvPollDone);
   float best = -INFINITY;
   int bidx = 0x7fffffff;
 #pragma unroll
@@ -371,11 +480,13 @@ __device__ __forceinline__ bool sample_greedy(const DraftArgs& p, int r, int ste
     bidx = 0;
   }
   if (lane == 0) {
+    if (r == static_cast<int>(blockIdx.x)) DRAFT_TRACE(p, step, kEvPicked);
     p.tokens[out] = bidx;
     p.pd_tok[out] = 1.0f;
     p.logZ[out] = best;
   }
   publish_token(p, r, step, bidx);
+  if (lane == 0 && r == static_cast<int>(blockIdx.x)) DRAFT_TRACE(p, step, kEvPublished);
   return true;
 }
 
@@ -430,6 +541,8 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
     constexpr int KC = kEntriesPerLane;
     unsigned long long ent[KC];
     const bool ok = poll_row(p, r, static_cast<uint32_t>(step + 1), ent);
+    const bool traced = lane == 0 && r == static_cast<int>(blockIdx.x);
+    if (traced) DRAFT_TRACE(p, step, kEvPollDone);
     int state = kSlotAbort, sstar = 0;
     float M = 0.f, Z = 0.f, target = 0.f, before_s = 0.f;
     if (ok) {
@@ -466,20 +579,22 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
         const int tb = chunk_first_tile(cc.idx, p.n_tiles, p.n_chunks);
         const int te = chunk_first_tile(cc.idx + 1, p.n_tiles, p.n_chunks);
         const int nsub = 2 * (te - tb);  // <= kMaxSampleChunks (host check)
-        float2 f[KC];
-#pragma unroll
-        for (int k = 0; k < KC; ++k) {
-          const int i = k * 32 + lane;
-          f[k] = i < nsub ? __ldcg(p.fine + static_cast<size_t>(2 * tb + i) * p.R_pad + r) : make_float2(-INFINITY, 0.f);
-        }
+        unsigned long long fw[KC];
+        const bool fine_ok = load_fine(p, r, 2 * tb, nsub, static_cast<uint32_t>(step + 1), fw);
         __syncwarp();  // every lane is done reading the chunk weights
 #pragma unroll
-        for (int k = 0; k < KC; ++k) sm.wts[k * 32 + lane] = f[k].x > -INFINITY ? f[k].y * ex2(f[k].x - M) : 0.f;
+        for (int k = 0; k < KC; ++k) {
+          // each sub-tile's mass in units of 2^M
+          const float o = __uint_as_float(static_cast<uint32_t>(fw[k]));
+          const float sw = __uint_as_float(static_cast<uint32_t>(fw[k] >> 32));
+          sm.wts[k * 32 + lane] = sw > 0.f ? sw * ex2(o - M) : 0.f;
+        }
         __syncwarp();
         const Crossing cs = warp_crossing(sm.wts, nsub, cc.before, target);
         sstar = 2 * tb + cs.idx;
         before_s = cs.before;
-        if (lane == 0) {
+        if (!fine_ok) state = kSlotAbort;
+        if (lane == 0 && fine_ok) {
           // the previous request's readers of the slab are past the barrier
           fence_proxy_async_smem();
           // W2[:, v0 .. v0+31] (columns past V zero-filled) and U[r, step, v0 .. v0+31]
@@ -488,6 +603,7 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
           mbar_arrive_expect_tx(sm.bar, static_cast<uint32_t>(p.rank) * 64u + ubytes);
           tma_load_2d(sm.slab_s, tm_slab, sm.bar, v0, 0, policy_evict_normal());
           bulk_load(sm.slab_s + p.rank * 64, p.U + out * p.V + v0, ubytes, sm.bar, policy_evict_first());
+          if (traced) DRAFT_TRACE(p, step, kEvSlabIssued);
         }
       }
     }
@@ -508,6 +624,7 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
   if (state == kSlotSample) {
     landed = __all_sync(0xffffffffu, mbar_wait(sm.bar, phase & 1u, abort_flag));
     if (!landed) *abort_flag = 1;
+    if (sub == 0 && lane == 0 && r == static_cast<int>(blockIdx.x)) DRAFT_TRACE(p, step, kEvSlabLanded);
     // this warp's share of the 32 bias values: lane l sums column v0 + l over
     // the warp's rank rows (W1 entries read as shared-memory broadcasts)
     float acc = 0.f;
@@ -559,12 +676,14 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
       const float ypick = __shfl_sync(0xffffffffu, y, pick);
       x = min(v0 + pick, p.V - 1);
       if (lane == 0) {
+        if (r == static_cast<int>(blockIdx.x)) DRAFT_TRACE(p, step, kEvPicked);
         p.tokens[out] = x;
         p.pd_tok[out] = __fdividef(ex2(ypick - M), Z);
         p.logZ[out] = (M + __log2f(Z)) * 0.69314718f;
       }
     }
     publish_token(p, r, step, x);
+    if (lane == 0 && r == static_cast<int>(blockIdx.x)) DRAFT_TRACE(p, step, kEvPublished);
   }
   // the slot, the shares and the slab are rewritten for the next request only
   // after that request's first barrier, which the leader reaches only after
@@ -572,26 +691,37 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
   return state == kSlotAbort ? -1 : (state == kSlotSample ? 1 : 0);
 }
 
-// Adds tile `it`'s U values (this thread's row, 32 columns of half h) to z
-// once the tile's U stage has landed, then releases the stage.  False when the
-// wait gave up.
-__device__ __forceinline__ bool add_u_tile(float (&z)[32], uint32_t bar_ufull, uint32_t bar_uempty, const uint8_t* u0,
-                                           int row, int h, int it, volatile int* abort_flag) {
-  const int lane = threadIdx.x & 31;
-  const int su = it % kDraftUStages;
-  if (!__all_sync(0xffffffffu, mbar_wait(bar_ufull + 8 * su, (it / kDraftUStages) & 1, abort_flag))) return false;
-  const float4* urow = reinterpret_cast<const float4*>(u0 + su * kDraftUBytes + row * (kDraftUCols * 4) + h * (kSubN * 4));
+// 5-D tiled tensor load (coordinates in elements, innermost first).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0, int32_t c1,
+                                            int32_t c2, int32_t c3, int32_t c4, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar), "l"(policy)
+      : "memory");
+}
+// Shared memory -> tensor memory, 128 lanes x 256 bits (8 fp32 columns), one
+// thread; completion through tcgen05.commit.  A later MMA that accumulates
+// into the same columns is NOT ordered after it: wait on the commit first.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Whether the U tile starting at column v0 uses the fast 5-D layout (see
+// kDraftUBytes): R a multiple of 8 and the whole tile inside the vocabulary.
+__device__ __forceinline__ bool u_fast_tile(const DraftArgs& p, int v0) { return (p.R & 7) == 0 && v0 + kTileN <= p.V; }
+
+// Copies one U tile from its shared-memory stage into 64 accumulator columns
+// (8 copies of 32 bytes per row), in the tile's layout.
+__device__ __forceinline__ void copy_u_tile(uint32_t stage, uint32_t dst_col, bool fast) {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float4 t4 = urow[k];
-    z[4 * k] += t4.x; z[4 * k + 1] += t4.y; z[4 * k + 2] += t4.z; z[4 * k + 3] += t4.w;
-  }
-  // the stage is refilled by TMA (async proxy) once released: order these
-  // generic-proxy reads before that write
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar_uempty + 8 * su);
-  return true;
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint64_t desc = fast ? smem_desc_sw128(stage + h * 1024 + k * 32, 16, 2048)
+                                 : smem_desc_sw128(stage + h * 16384 + k * 32, 16, 1024);
+      tmem_cp_128x256b(dst_col + h * 32 + k * 8, desc);
+    }
 }
 
 // Folds a sub-tile partial (max y, sum exp2(y - max y)) into a running one.
@@ -608,8 +738,9 @@ __device__ __forceinline__ void merge_partial(float mx, float sm, float& runM, f
 
 template <bool kGreedy>
 __global__ void __launch_bounds__(kDraftKThreads, 1)
-    k_markov_draft(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u,
-                   const __grid_constant__ CUtensorMap tm_slab, const DraftArgs p) {
+    k_markov_draft(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u5,
+                   const __grid_constant__ CUtensorMap tm_u3, const __grid_constant__ CUtensorMap tm_slab,
+                   const DraftArgs p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -632,9 +763,11 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
   const uint32_t bar_uempty = bar_ufull + 8 * kDraftUStages;  // [kDraftUStages]
   const uint32_t bar_tfull = bar_uempty + 8 * kDraftUStages;   // [kDraftAccPairs]
   const uint32_t bar_tempty = bar_tfull + 8 * kDraftAccPairs;  // [kDraftAccPairs]
-  const uint32_t bar_slab = bar_tempty + 8 * kDraftAccPairs;   // the sampler's slab copies
-  const uint32_t bar_drain = bar_slab + 8;                     // the MMA issuer's last commit on abort
-  constexpr uint32_t kBarBytes = 16 * (kDraftWStages + kDraftUStages + kDraftAccPairs) + 16;
+  const uint32_t bar_ucopied = bar_tempty + 8 * kDraftAccPairs;  // [kDraftAccPairs] U copied into the pair
+  const uint32_t bar_slab = bar_ucopied + 8 * kDraftAccPairs;   // the sampler's slab copies
+  const uint32_t bar_drain = bar_slab + 8;                      // the MMA issuer's last commit on abort
+  const uint32_t bar_cdrain = bar_drain + 8;                    // the copier's last commit
+  constexpr uint32_t kBarBytes = 16 * (kDraftWStages + kDraftUStages) + 24 * kDraftAccPairs + 24;
   static_assert(kBarBytes + 8 <= 256, "barrier block");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + plan.bars + kBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + plan.bars + kBarBytes + 4);
@@ -647,18 +780,21 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
     }
     for (int s = 0; s < kDraftUStages; ++s) {
       mbar_init(bar_ufull + 8 * s, 1);
-      mbar_init(bar_uempty + 8 * s, 8);
+      mbar_init(bar_uempty + 8 * s, 1);  // the copier's commit
     }
     for (int s = 0; s < kDraftAccPairs; ++s) {
       mbar_init(bar_tfull + 8 * s, 1);
       mbar_init(bar_tempty + 8 * s, 8);
+      mbar_init(bar_ucopied + 8 * s, 1);
     }
     mbar_init(bar_slab, 1);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_cdrain, 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tm_w2);
-    prefetch_tensormap(&tm_u);
+    if ((p.R & 7) == 0) prefetch_tensormap(&tm_u5);
+    prefetch_tensormap(&tm_u3);
     prefetch_tensormap(&tm_slab);
   }
   if (warp == 1) {
@@ -728,9 +864,14 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
           *abort_flag = 1;
           break;
         }
-        // one 128-row x 68-column box; rows past R and columns past V are zero-filled
+        // rows past R and columns past V are zero-filled
         mbar_arrive_expect_tx(bar_ufull + 8 * su, kDraftUBytes);
-        tma_load_3d(base + plan.u(su), &tm_u, bar_ufull + 8 * su, v0, step, r0, pol_u);
+        if (u_fast_tile(p, v0)) {
+          tma_load_5d(base + plan.u(su), &tm_u5, bar_ufull + 8 * su, 0, 0, v0 / 32, r0 / 8, step, pol_u);
+        } else {
+          tma_load_3d(base + plan.u(su), &tm_u3, bar_ufull + 8 * su, v0, step, r0, pol_u);
+          tma_load_3d(base + plan.u(su) + 16384, &tm_u3, bar_ufull + 8 * su, v0 + 32, step, r0, pol_u);
+        }
         ++ufilled;
       }
       if (*abort_flag) {
@@ -739,6 +880,50 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
           while (!mbar_try_wait(bar_ufull + 8 * (i % kDraftUStages), (i / kDraftUStages) & 1) &&
                  global_ns() - t0 < kWaitLimitNs) {
           }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kCopyWarp) {
+    // ---------------------------------------------------------- U copier (all positions, lane 0)
+    // Each tile's U goes from its ring stage into its accumulator pair once the
+    // epilogue has drained that pair's previous use; the commit after a tile
+    // frees its stage, the one after a pair's last tile lets the MMA in.
+    if (lane == 0) {
+      int issued = 0;
+      for (int gp = 0; gp < npair * p.gamma; ++gp) {
+        const int step = gp / npair, j = gp - step * npair, pa = gp % kDraftAccPairs;
+        if (!mbar_wait(bar_tempty + 8 * pa, ((gp / kDraftAccPairs) & 1) ^ 1, abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after_sync();
+        const int ntp = 2 * j + 1 < ntile ? 2 : 1;
+        bool ok = true;
+        for (int t = 0; t < ntp; ++t) {
+          const int it = step * ntile + 2 * j + t;
+          const int su = it % kDraftUStages;
+          if (!mbar_wait(bar_ufull + 8 * su, (it / kDraftUStages) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int v0 = (t_begin + tile_of(step, 2 * j + t, ntile)) * kTileN;
+          copy_u_tile(base + plan.u(su), tmem_base + static_cast<uint32_t>(pa * 2 * kTileN + t * kTileN),
+                      u_fast_tile(p, v0));
+          umma_commit(bar_uempty + 8 * su);
+          issued = 1;
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+        umma_commit(bar_ucopied + 8 * pa);
+      }
+      if (issued) {
+        // every copy this thread issued is complete before tensor memory is freed
+        umma_commit(bar_cdrain);
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(bar_cdrain, 0) && global_ns() - t0 < kWaitLimitNs) {
+        }
       }
     }
     __syncwarp();
@@ -754,7 +939,8 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
         bool ok = true;
         for (int j = 0; j < npair && ok; ++j) {
           const int gp = step * npair + j, pa = gp % kDraftAccPairs;
-          if (!mbar_wait(bar_tempty + 8 * pa, ((gp / kDraftAccPairs) & 1) ^ 1, abort_flag)) {
+          // the pair's U is in its accumulator (the copier waited for the drain)
+          if (!mbar_wait(bar_ucopied + 8 * pa, (gp / kDraftAccPairs) & 1, abort_flag)) {
             *abort_flag = 1;
             break;
           }
@@ -775,7 +961,7 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
               // N-direction atom stride (LBO) = one box: the pair's second tile
               const uint32_t b_addr = base + plan.w(sw) + q4 * 2048;
               const int ks = kc * (kDraftKChunk / 16) + q4;
-              umma_bf16_ts(d, tmem_a + ks * 8, smem_desc_sw128(b_addr, kDraftWBox, 1024), idesc, ks > 0 ? 1u : 0u);
+              umma_bf16_ts(d, tmem_a + ks * 8, smem_desc_sw128(b_addr, kDraftWBox, 1024), idesc, 1u);  // onto U
             }
             umma_commit(bar_wempty + 8 * sw);
             issued = 1;
@@ -820,6 +1006,7 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
         if (threadIdx.x == 64 && !*abort_flag &&
             !wait_at_least(p.ready + 16 * mtile, static_cast<uint32_t>(rows_valid * step), p.abort))
           *abort_flag = 1;
+        if (threadIdx.x == 64) DRAFT_TRACE(p, step, kEvReadySeen);
         named_barrier(4, kEpiThreads);
       }
       if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
@@ -865,6 +1052,7 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
       }
       tc_fence_before_sync();
       named_barrier(2, kEpiThreads + 32);
+      if (threadIdx.x == 64) DRAFT_TRACE(p, step, kEvAReady);
 
       // ---- tiles
       float runM = -INFINITY, runS = 0.f;  // running (max, sum exp2) of this warp's half of the chunk
@@ -875,13 +1063,13 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
         for (int j = 0; j < npair; ++j) {
           const int i0 = 2 * j;
           const bool two = i0 + 1 < ntile;
-          const int it0 = step * ntile + i0;
           const int gp = step * npair + j, pa = gp % kDraftAccPairs;
           if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * pa, (gp / kDraftAccPairs) & 1, abort_flag))) {
             *abort_flag = 1;
             break;
           }
           tc_fence_after_sync();
+          if (j == 0 && threadIdx.x == 64) DRAFT_TRACE(p, step, kEvFirstAcc);
           uint32_t a0[32], a1[32];
           const uint32_t tacc = tmem_base + lane_off + static_cast<uint32_t>(2 * pa * kTileN + h * kSubN);
           tmem_ld_32x32_nowait(tacc, a0);
@@ -891,16 +1079,12 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_tempty + 8 * pa);
+          // z = U + bias: the accumulators started from U
           float z0[32], z1[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
             z0[k] = __uint_as_float(a0[k]);
             z1[k] = __uint_as_float(a1[k]);
-          }
-          if (!add_u_tile(z0, bar_ufull, bar_uempty, gbase + plan.u0, row, h, it0, abort_flag) ||
-              (two && !add_u_tile(z1, bar_ufull, bar_uempty, gbase + plan.u0, row, h, it0 + 1, abort_flag))) {
-            *abort_flag = 1;
-            break;
           }
 
           // z = bias + U of 32 columns of each tile; columns past V only in the
@@ -919,42 +1103,40 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
 #pragma unroll
             for (int k = 0; k < 32; ++k) z1[k] = k < ncol1 ? z1[k] : -INFINITY;
           }
-          const size_t f0 = static_cast<size_t>(2 * (t_begin + ti0) + h) * p.R_pad + r;
-          const size_t f1 = static_cast<size_t>(2 * (t_begin + ti1) + h) * p.R_pad + r;
           if constexpr (kGreedy) {
             int k0, k1;
             const float mx0 = tree_argmax32(z0, &k0);
             const float mx1 = tree_argmax32(z1, &k1);
             const int ix0 = v00 + k0, ix1 = v01 + k1;
-            if (valid) p.fine[f0] = make_float2(mx0, __int_as_float(ix0));
-            if (valid && two) p.fine[f1] = make_float2(mx1, __int_as_float(ix1));
             if (mx0 > runM || (mx0 == runM && ix0 < runIdx)) { runM = mx0; runIdx = ix0; }
             if (two && (mx1 > runM || (mx1 == runM && ix1 < runIdx))) { runM = mx1; runIdx = ix1; }
           } else {
-            // y = z * log2(e)/T; partial (max y, sum exp2(y - max y)); an
-            // all-empty sub-tile gives (-inf, 0)
-            const float mz0 = tree_max32(z0), mz1 = tree_max32(z1);
-            const float mx0 = mz0 * p.scale, mx1 = mz1 * p.scale;
-            const float o0 = mz0 > -INFINITY ? mx0 : 0.f, o1 = mz1 > -INFINITY ? mx1 : 0.f;
+            // y = z * log2(e)/T; partial (o, sum 2^(y - o)) with o the tagged
+            // maximum (fine_ref); an all-empty sub-tile gives sum 0
+            const uint32_t ftag = static_cast<uint32_t>(step + 1);
+            const float o0 = fine_ref(tree_max32(z0) * p.scale, ftag), o1 = fine_ref(tree_max32(z1) * p.scale, ftag);
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
               z0[k] = ex2(fmaf(z0[k], p.scale, -o0));
               z1[k] = ex2(fmaf(z1[k], p.scale, -o1));
             }
             const float sm0 = tree_sum32(z0), sm1 = tree_sum32(z1);
-            if (valid) p.fine[f0] = make_float2(mx0, sm0);
-            if (valid && two) p.fine[f1] = make_float2(mx1, sm1);
-            merge_partial(mx0, sm0, runM, runS);
-            merge_partial(mx1, sm1, runM, runS);
+            const size_t f0 = static_cast<size_t>(2 * (t_begin + ti0) + h) * p.R_pad + r;
+            const size_t f1 = static_cast<size_t>(2 * (t_begin + ti1) + h) * p.R_pad + r;
+            if (valid) st_relaxed_gpu_u64(p.fine + f0, fine_word(o0, sm0));
+            if (valid && two) st_relaxed_gpu_u64(p.fine + f1, fine_word(o1, sm1));
+            merge_partial(o0, sm0, runM, runS);
+            merge_partial(o1, sm1, runM, runS);
           }
         }
       }
+      if (threadIdx.x == 64) DRAFT_TRACE(p, step, kEvTilesDone);
       // ---- combine the two column halves of this CTA's chunk
       if (h == 1) s_half[row] = kGreedy ? make_float2(runM, __int_as_float(runIdx)) : make_float2(runM, runS);
       named_barrier(1, kEpiThreads);
       if (h == 0 && valid && !*abort_flag) {
-        // publish the row's chunk entry: one release store, after the barrier
-        // above has made both halves' sub-tile partials part of this thread's view
+        // publish the row's chunk entry: one relaxed store (its tag is all a
+        // reader checks)
         const float2 o = s_half[row];
         unsigned long long ent;
         if constexpr (kGreedy) {
@@ -972,8 +1154,9 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
           const float L = Mx > -INFINITY ? Mx + __log2f(S) : -INFINITY;
           ent = chunk_entry(L, static_cast<uint32_t>(step + 1), 0u);
         }
-        st_release_gpu_u64(p.centry + static_cast<size_t>(r) * p.n_chunks + chunk, ent);
+        st_relaxed_gpu_u64(p.centry + static_cast<size_t>(r) * p.n_chunks + chunk, ent);
       }
+      if (threadIdx.x == 64) DRAFT_TRACE(p, step, kEvEntry);
 
       // ---- sample this CTA's requests once every chunk of their M-tile is done
       if constexpr (kGreedy) {
@@ -1065,20 +1248,46 @@ int encode_w2_slab_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank) {
   return rc == CUDA_SUCCESS ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
+// U [R, gamma, V] fp32 as a 5-D tensor for the fast tile layout (R % 8 == 0):
+// (32 columns, 8 rows of a row group, 32-column block, row group, position),
+// box {32, 8, 2, 16, 1} with 128-byte swizzle: one 64-column tile of 128 rows
+// per load, each row's 256 bytes fetched together, half h of row group g at
+// byte g * 2048 + h * 1024.  Only whole tiles are loaded through it.
+static int encode_u_fast_map(CUtensorMap* tm, const float* U, int R, int gamma, int V) {
+  auto fn = get_encode_fn();
+  if (!fn) return DSPARK_ERR_CUDA;
+  const cuuint64_t row = static_cast<cuuint64_t>(V) * 4 * gamma;  // bytes between requests
+  cuuint64_t dims[5] = {32, 8, static_cast<cuuint64_t>(V / 32), static_cast<cuuint64_t>(R / 8),
+                        static_cast<cuuint64_t>(gamma)};
+  cuuint64_t strides[4] = {row, 128, 8 * row, static_cast<cuuint64_t>(V) * 4};
+  cuuint32_t box[5] = {32, 8, 2, static_cast<cuuint32_t>(kMTile / 8), 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult rc = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, const_cast<float*>(U), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
 // U [R, gamma, V] fp32 as a 3-D tensor (x = vocabulary, y = position,
-// z = request); box 68 x 1 x 128, no swizzle (see kDraftUCols).
-int encode_u_map(CUtensorMap* tm, const float* U, int R, int gamma, int V) {
+// z = request), box {32, 1, 128} with 128-byte swizzle: one 32-column half of
+// a tile (the general layout), columns past V and rows past R zero-filled.
+static int encode_u_half_map(CUtensorMap* tm, const float* U, int R, int gamma, int V) {
   auto fn = get_encode_fn();
   if (!fn) return DSPARK_ERR_CUDA;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(gamma), static_cast<cuuint64_t>(R)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(V) * 4, static_cast<cuuint64_t>(V) * 4 * gamma};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kDraftUCols), 1, static_cast<cuuint32_t>(kMTile)};
+  cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(kMTile)};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult rc = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(U), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return rc == CUDA_SUCCESS ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
+
+#ifdef DSPARK_DRAFT_TRACE
+static unsigned long long* g_trace = nullptr;
+static size_t g_trace_bytes = 0;
+#endif
 
 int vocab_chunks(int n_tiles, int n_mtiles) {
   int c = sm_count() / n_mtiles;
@@ -1097,13 +1306,16 @@ int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
   a.U = U; a.W1 = W1; a.W2 = W2; a.anchors = anchors;
   a.tokens = tokens; a.pd_tok = pd_tok; a.logZ = logZ;
   a.centry = reinterpret_cast<unsigned long long*>(ws + L.coarse);
-  a.fine = reinterpret_cast<float2*>(ws + L.fine);
+  a.fine = reinterpret_cast<unsigned long long*>(ws + L.fine);
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
   a.R = R;
   a.n_mtiles = ceil_div(R, kMTile);
   a.ready = reinterpret_cast<uint32_t*>(ws + L.dsync) + 16 * a.n_mtiles;
   a.abort = a.ready + 16 * a.n_mtiles;
   a.abuf = reinterpret_cast<uint4*>(ws + L.abuf);
+#ifdef DSPARK_DRAFT_TRACE
+  a.trace = nullptr;
+#endif
   a.R_pad = a.n_mtiles * kMTile;
   a.gamma = gamma; a.V = V; a.rank = rank;
   a.n_tiles = ceil_div(V, kTileN);
@@ -1116,8 +1328,10 @@ int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
   if (a.n_chunks > kMaxSampleChunks || 2 * ceil_div(a.n_tiles, a.n_chunks) > kMaxSampleChunks || V > kMaxDraftV)
     return DSPARK_ERR_UNSUPPORTED_SHAPE;
 
-  CUtensorMap tm_w2, tm_u, tm_slab;
-  if (encode_w2_kchunk_map(&tm_w2, W2, V, rank) != DSPARK_OK || encode_u_map(&tm_u, U, R, gamma, V) != DSPARK_OK ||
+  CUtensorMap tm_w2, tm_u5, tm_u3, tm_slab;
+  std::memset(&tm_u5, 0, sizeof(tm_u5));  // not used unless R % 8 == 0
+  if (encode_w2_kchunk_map(&tm_w2, W2, V, rank) != DSPARK_OK || encode_u_half_map(&tm_u3, U, R, gamma, V) != DSPARK_OK ||
+      ((R & 7) == 0 && encode_u_fast_map(&tm_u5, U, R, gamma, V) != DSPARK_OK) ||
       encode_w2_slab_map(&tm_slab, W2, V, rank) != DSPARK_OK)
     return DSPARK_ERR_CUDA;
 
@@ -1126,12 +1340,19 @@ int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
   auto kernel = greedy ? k_markov_draft<true> : k_markov_draft<false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess)
     return DSPARK_ERR_CUDA;
-  // the chunk entries (no tag matches), the ready counters and the abort word
-  // start at zero on every call
+  // the chunk entries and the sub-tile partials (no tag matches), the ready
+  // counters and the abort word start at zero on every call
   if (cudaMemsetAsync(ws + L.coarse, 0, static_cast<size_t>(a.R_pad) * a.n_chunks * 8, stream) != cudaSuccess ||
-      cudaMemsetAsync(ws + L.dsync, 0, L.dsync_bytes, stream) != cudaSuccess)
+      cudaMemsetAsync(ws + L.dsync, 0, L.dsync_bytes, stream) != cudaSuccess ||
+      (!greedy && cudaMemsetAsync(ws + L.fine, 0, static_cast<size_t>(2 * a.n_tiles) * a.R_pad * 8, stream) != cudaSuccess))
     return DSPARK_ERR_CUDA;
 
+#ifdef DSPARK_DRAFT_TRACE
+  if (g_trace && g_trace_bytes >= static_cast<size_t>(gamma) * a.n_chunks * a.n_mtiles * kTraceEvents * 8) {
+    a.trace = g_trace;
+    if (cudaMemsetAsync(g_trace, 0, g_trace_bytes, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  }
+#endif
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks * a.n_mtiles);
   cfg.blockDim = dim3(kDraftKThreads);
@@ -1142,7 +1363,17 @@ int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tm_w2, tm_u, tm_slab, a) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kernel, tm_w2, tm_u5, tm_u3, tm_slab, a) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
 }  // namespace dspark
+
+#ifdef DSPARK_DRAFT_TRACE
+// Traced build only: the device buffer the next draft calls stamp their phase
+// times into ([gamma][n_ctas][kTraceEvents] uint64; too small = no tracing).
+extern "C" int dspark_draft_trace_buffer(void* buf, size_t bytes) {
+  dspark::g_trace = static_cast<unsigned long long*>(buf);
+  dspark::g_trace_bytes = buf ? bytes : 0;
+  return DSPARK_OK;
+}
+#endif

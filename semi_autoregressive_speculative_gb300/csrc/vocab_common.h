@@ -19,8 +19,6 @@ int encode_w2_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank);
 // W2 again, box 32 x rank without swizzle: the 32 columns of one sub-tile as
 // [rank][32] (the samplers' recompute of a sub-tile's bias).
 int encode_w2_slab_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank);
-// U [R, gamma, V] fp32 as a 3-D tensor; box 68 x 1 x 128, no swizzle.
-int encode_u_map(CUtensorMap* tm, const float* U, int R, int gamma, int V);
 // Contiguous V-chunks per M-tile so that chunks x M-tiles fills the SMs once.
 int vocab_chunks(int n_tiles, int n_mtiles);
 
