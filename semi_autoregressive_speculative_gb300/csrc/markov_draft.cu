@@ -58,8 +58,8 @@ namespace dspark {
 // its 4 MMAs are done, so the ring keeps most of its bytes in flight.
 constexpr int kDraftKChunk = 64;     // rank rows per W2 stage
 constexpr int kDraftWBox = kDraftKChunk * 128;  // bytes of one 64-column box of a stage
-constexpr int kDraftWStages = 6;     // W2 K-chunk stages (L2-resident after the first position)
-constexpr int kDraftUStages = 3;     // U tiles in flight per CTA (the HBM stream)
+constexpr int kDraftWStages = 8;     // W2 K-chunk stages (L2-resident after the first position)
+constexpr int kDraftUStages = 2;     // U tiles staged in shared memory (tensor memory holds 3 pairs more)
 constexpr int kDraftAccPairs = 3;    // fp32 accumulator pairs (2 x 64 columns each) in tensor memory
 constexpr int kDraftACol = kDraftAccPairs * 2 * kTileN;  // first tensor-memory column of the A operand
 constexpr int kDraftTmemCols = 512;                      // accumulators + A (rank / 2 <= 128 columns)
@@ -99,12 +99,16 @@ enum TraceEvent {
   kEvTilesDone = 2,   // the CTA's last tile pair of the position is reduced
   kEvEntry = 3,       // the CTA's chunk entries are published
   kEvPollDone = 4,    // sampler (the CTA's first request): every chunk entry seen
-  kEvSlabIssued = 5,  // sampler: crossing sub-tile found, slab copy issued
-  kEvSlabLanded = 6,  // sampler: slab in shared memory
-  kEvPicked = 7,      // sampler: token picked
-  kEvPublished = 8,   // sampler: token published (W1 row staged, counted)
-  kEvReadySeen = 9,   // the previous position's tokens of the M-tile are all published
-  kTraceEvents = 10
+  kEvChunkFound = 5,  // sampler: crossing chunk found
+  kEvFineLoaded = 6,  // sampler: the crossing chunk's sub-tile partials loaded
+  kEvSlabIssued = 7,  // sampler: crossing sub-tile found, slab copy issued
+  kEvSlabLanded = 8,  // sampler: slab in shared memory
+  kEvPicked = 9,      // sampler: token picked
+  kEvPublished = 10,  // sampler: token published (W1 row staged, counted)
+  kEvReadySeen = 11,  // the previous position's tokens of the M-tile are all published
+  kEvCopyFirst = 12,  // copier: the position's first pair of U is in tensor memory (issued)
+  kEvCopyThird = 13,  // copier: the position's third pair of U is in tensor memory (issued)
+  kTraceEvents = 14
 };
 #ifdef DSPARK_DRAFT_TRACE
 #define DRAFT_TRACE(p, step, ev)                                                                         \
@@ -155,7 +159,7 @@ __host__ __device__ inline DraftSmem draft_smem_plan(int rank) {
   s.w0 = off; s.wstride = 2u * kDraftWBox; off += kDraftWStages * s.wstride;  // 2 x (64 rows x 64 bf16), SW128
   s.u0 = off; off += kDraftUStages * kDraftUBytes;
   s.half = off; off += kMTile * 8;
-  s.bars = off; off += 256;
+  s.bars = off; off += 320;
   s.slots = off; off += 32;                      // the sampler's SampleSlot
   s.part = off; off += 8 * 32 * 4;               // each epilogue warp's 32 column shares
   s.wts = off; off += kMaxSampleChunks * 4;      // the leader's search weights
@@ -318,7 +322,9 @@ __device__ __forceinline__ float tree_argmax32(const float (&z)[32], int* idx) {
 // Publishes request r's token x (one warp): copies W1[x] into the row's slot
 // of the A-operand staging buffer, in the order the gather reads it (for each
 // 16-byte piece k, the 32 rows of a lane quarter are contiguous, so a gather
-// warp reads whole 128-byte lines), then lane 0 counts the token on the M-tile.
+// warp reads whole 128-byte lines), then lane 0 counts the token on the M-tile
+// (a release fence, then a relaxed add: the ready counter's pollers pair it
+// with their own acquire).
 __device__ __forceinline__ void publish_token(const DraftArgs& p, int r, int step, int x) {
   if (step + 1 >= p.gamma) return;
   const int lane = threadIdx.x & 31;
@@ -330,8 +336,8 @@ __device__ __forceinline__ void publish_token(const DraftArgs& p, int r, int ste
   }
   __syncwarp();
   if (lane == 0) {
-    __threadfence();
-    atomicAdd(p.ready + 16 * (r / kMTile), 1u);
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(p.ready + 16 * (r / kMTile)) : "memory");
   }
 }
 
@@ -372,9 +378,10 @@ constexpr int kEntriesPerLane = kMaxSampleChunks / 32;
 
 // One warp waits until every chunk entry of row r carries `tag`; lane l gets
 // the entries of chunks k * 32 + l in e[k] (0 past n_chunks).  Polls with a
-// relaxed load per pending entry (all in flight together) and a short sleep;
-// gives up (false, the same in every lane, abort word raised) after
-// kWaitLimitNs or on abort.
+// relaxed load per pending entry, two rounds in flight (a round is checked
+// while the next is already issued, which halves the time between an entry
+// landing and its round returning); gives up (false, the same in every lane,
+// abort word raised) after kWaitLimitNs or on abort.
 __device__ __forceinline__ bool poll_row(const DraftArgs& p, int r, uint32_t tag,
                                          unsigned long long (&e)[kEntriesPerLane]) {
   const int lane = threadIdx.x & 31;
@@ -386,16 +393,21 @@ __device__ __forceinline__ bool poll_row(const DraftArgs& p, int r, uint32_t tag
     if (k * 32 + lane < p.n_chunks) pending |= 1u << k;
   }
   const uint64_t t0 = global_ns();
+  unsigned long long prev[kEntriesPerLane];
+#pragma unroll
+  for (int k = 0; k < kEntriesPerLane; ++k) prev[k] = (pending & (1u << k)) ? ld_relaxed_gpu_u64(row + k * 32 + lane) : 0ull;
   for (uint32_t it = 0;; ++it) {
+    // the next round is in flight while the previous one is checked
+    unsigned long long cur[kEntriesPerLane];
+#pragma unroll
+    for (int k = 0; k < kEntriesPerLane; ++k) cur[k] = (pending & (1u << k)) ? ld_relaxed_gpu_u64(row + k * 32 + lane) : 0ull;
 #pragma unroll
     for (int k = 0; k < kEntriesPerLane; ++k) {
-      if (pending & (1u << k)) {
-        const unsigned long long v = ld_relaxed_gpu_u64(row + k * 32 + lane);
-        if (static_cast<uint32_t>(v >> 56) == tag) {
-          e[k] = v;
-          pending &= ~(1u << k);
-        }
+      if ((pending & (1u << k)) && static_cast<uint32_t>(prev[k] >> 56) == tag) {
+        e[k] = prev[k];
+        pending &= ~(1u << k);
       }
+      prev[k] = cur[k];
     }
     if (__all_sync(0xffffffffu, pending == 0)) break;
     if ((it & 15u) == 15u) {
@@ -406,7 +418,6 @@ __device__ __forceinline__ bool poll_row(const DraftArgs& p, int r, uint32_t tag
         return false;
       }
     }
-    __nanosleep(32);
   }
   __syncwarp();
   return true;
@@ -579,8 +590,10 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
         const int tb = chunk_first_tile(cc.idx, p.n_tiles, p.n_chunks);
         const int te = chunk_first_tile(cc.idx + 1, p.n_tiles, p.n_chunks);
         const int nsub = 2 * (te - tb);  // <= kMaxSampleChunks (host check)
+        if (traced) DRAFT_TRACE(p, step, kEvChunkFound);
         unsigned long long fw[KC];
         const bool fine_ok = load_fine(p, r, 2 * tb, nsub, static_cast<uint32_t>(step + 1), fw);
+        if (traced) DRAFT_TRACE(p, step, kEvFineLoaded);
         __syncwarp();  // every lane is done reading the chunk weights
 #pragma unroll
         for (int k = 0; k < KC; ++k) {
@@ -768,7 +781,7 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
   const uint32_t bar_drain = bar_slab + 8;                      // the MMA issuer's last commit on abort
   const uint32_t bar_cdrain = bar_drain + 8;                    // the copier's last commit
   constexpr uint32_t kBarBytes = 16 * (kDraftWStages + kDraftUStages) + 24 * kDraftAccPairs + 24;
-  static_assert(kBarBytes + 8 <= 256, "barrier block");
+  static_assert(kBarBytes + 8 <= 320, "barrier block");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + plan.bars + kBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + plan.bars + kBarBytes + 4);
   float2* s_half = reinterpret_cast<float2*>(gbase + plan.half);
@@ -917,6 +930,8 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
           break;
         }
         umma_commit(bar_ucopied + 8 * pa);
+        if (j == 0) DRAFT_TRACE(p, step, kEvCopyFirst);
+        if (j == 2) DRAFT_TRACE(p, step, kEvCopyThird);
       }
       if (issued) {
         // every copy this thread issued is complete before tensor memory is freed

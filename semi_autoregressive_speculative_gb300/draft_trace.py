@@ -22,8 +22,8 @@ import numpy as np
 from . import build as pkg_build
 from . import synth
 
-EVENTS = ["a_ready", "first_acc", "tiles_done", "entry", "poll_done", "slab_issued", "slab_landed", "picked",
-          "published", "ready_seen"]
+EVENTS = ["a_ready", "first_acc", "tiles_done", "entry", "poll_done", "chunk_found", "fine_loaded", "slab_issued",
+          "slab_landed", "picked", "published", "ready_seen", "copy_first", "copy_third"]
 K_MTILE, K_TILE_N, K_MAX_CHUNKS = 128, 64, 1024
 
 
@@ -50,7 +50,7 @@ def grid_size(R: int, V: int, sm_count: int) -> int:
 
 
 def phases(tr: np.ndarray, R: int) -> dict:
-    """Median phase durations (µs) from stamps tr [gamma, n_ctas, 10] (ns)."""
+    """Median phase durations (µs) from stamps tr [gamma, n_ctas, len(EVENTS)] (ns)."""
     g, n, _ = tr.shape
     e = {name: tr[:, :, i].astype(np.float64) for i, name in enumerate(EVENTS)}
     samplers = np.arange(min(R, n))  # CTA c samples request c first
@@ -64,7 +64,9 @@ def phases(tr: np.ndarray, R: int) -> dict:
         "tiles_end_last_minus_median": us([e["tiles_done"][j].max() - np.median(e["tiles_done"][j]) for j in js]),
         "entry_publish": us([e["entry"][j] - e["tiles_done"][j] for j in js]),
         "poll_after_last_entry": us([e["poll_done"][j][samplers] - e["entry"][j].max() for j in js]),
-        "search_and_slab_issue": us([e["slab_issued"][j][samplers] - e["poll_done"][j][samplers] for j in js]),
+        "merge_and_chunk_search": us([e["chunk_found"][j][samplers] - e["poll_done"][j][samplers] for j in js]),
+        "fine_load": us([e["fine_loaded"][j][samplers] - e["chunk_found"][j][samplers] for j in js]),
+        "subtile_search_and_slab_issue": us([e["slab_issued"][j][samplers] - e["fine_loaded"][j][samplers] for j in js]),
         "slab_land": us([e["slab_landed"][j][samplers] - e["slab_issued"][j][samplers] for j in js]),
         "pick": us([e["picked"][j][samplers] - e["slab_landed"][j][samplers] for j in js]),
         "publish": us([e["published"][j][samplers] - e["picked"][j][samplers] for j in js]),
@@ -73,6 +75,10 @@ def phases(tr: np.ndarray, R: int) -> dict:
         # the chain from the last CTA's last tile to the next position's A operand, on the slowest path
         "chain_last_tile_to_next_a": us([e["a_ready"][j + 1].max() - e["tiles_done"][j].max() for j in js]),
         "last_entry_to_last_publish": us([e["published"][j][samplers].max() - e["entry"][j].max() for j in js]),
+        # the copier's lead: when the next position's first and third U pairs were in tensor memory,
+        # relative to this position's last tile (negative: before it)
+        "next_copy_first_after_tiles": us([e["copy_first"][j + 1] - e["tiles_done"][j] for j in js]),
+        "next_copy_third_after_tiles": us([e["copy_third"][j + 1] - e["tiles_done"][j] for j in js]),
     }
     return out
 
