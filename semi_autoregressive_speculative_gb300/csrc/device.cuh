@@ -203,6 +203,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
       : "memory");
 }
+// Four rows of a 2-D tensor (row coordinates r0..r3, the tensor map's box one
+// row high) at column x, stored one after another at dst; one instruction
+// for what would otherwise be four row copies.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, uint32_t bar, int32_t x, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
+      : "memory");
+}
 // Bring a 2-D tensor tile into L2 (with an eviction policy) without touching
 // shared memory.
 __device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int32_t y, uint64_t policy) {

@@ -1304,6 +1304,19 @@ static unsigned long long* g_trace = nullptr;
 static size_t g_trace_bytes = 0;
 #endif
 
+int encode_u_rows_map(CUtensorMap* tm, const float* U, int R, int gamma, int V) {
+  auto fn = get_encode_fn();
+  if (!fn) return DSPARK_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(R) * static_cast<cuuint64_t>(gamma)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), 1};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult rc = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(U), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
 int vocab_chunks(int n_tiles, int n_mtiles) {
   int c = sm_count() / n_mtiles;
   if (c < 1) c = 1;

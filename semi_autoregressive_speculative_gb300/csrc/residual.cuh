@@ -21,7 +21,9 @@
 // kernels that read the partials take the same split.
 //   warp 0     producer: W2 tiles by TMA (MN-major, 128B-swizzled) into a
 //              kStages-deep ring freed by the UMMA, and the gathered U rows by
-//              per-row bulk copies into a second ring freed by the epilogue;
+//              tile::gather4 loads (four rows per instruction: the TMA unit's
+//              issue rate, not HBM, bounds per-row copies) into a second ring
+//              freed by the epilogue;
 //   warp 1     allocates tensor memory and issues the UMMAs (one thread);
 //   warps 2-9  gather W1[x_i] into tensor memory as the A operand (one row per
 //              lane), then run the epilogue, two warps per tensor-memory lane
@@ -74,16 +76,17 @@ __host__ __device__ inline int residual_chunks(int rows, int grid, int n_tiles) 
 
 // Ring stages by arithmetic (w0 + s * wstride): a runtime-indexed array of
 // offsets would live in local memory.
+constexpr int kResURow = kTileN * 4;  // bytes per gathered U row in a stage (four rows per gather4)
 struct ResidualSmem {
   uint32_t w0, wstride, u0, half, bars, rows, total;
   __host__ __device__ uint32_t w(int s) const { return w0 + static_cast<uint32_t>(s) * wstride; }
-  __host__ __device__ uint32_t u(int s) const { return u0 + static_cast<uint32_t>(s) * (kMTile * kUStride); }
+  __host__ __device__ uint32_t u(int s) const { return u0 + static_cast<uint32_t>(s) * (kMTile * kResURow); }
 };
 __host__ __device__ inline ResidualSmem residual_smem_plan(int rank) {
   ResidualSmem s;
   uint32_t off = 0;
   s.w0 = off; s.wstride = 128u * rank; off += kStages * s.wstride;  // rank x 64 bf16, MN-major SW128
-  s.u0 = off; off += kStages * kMTile * kUStride;                     // 128 rows x 64 fp32, padded rows
+  s.u0 = off; off += kStages * kMTile * kResURow;                     // 128 rows x 64 fp32 (1024-aligned)
   s.half = off; off += kMTile * 8;   // second-half chunk partials
   s.bars = off; off += 256;          // mbarriers, tmem slot, abort flag
   s.rows = off; off += kMTile * 16;  // residual rows: token, request, position, fine column
@@ -92,7 +95,8 @@ __host__ __device__ inline ResidualSmem residual_smem_plan(int rank) {
 }
 
 __global__ void __launch_bounds__(kDraftThreads, 1)
-    k_residual_partials(const __grid_constant__ CUtensorMap tm_w2, const ResidualArgs p) {
+    k_residual_partials(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u,
+                        const ResidualArgs p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -138,6 +142,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tm_w2);
+    prefetch_tensormap(&tm_u);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -146,7 +151,6 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
   // residual rows: previous token, request, position, fine-partials column
   // (-1: none); a row with token -1 is idle (a bonus row j == gamma, which has
   // no draft distribution, or past the last row)
-  int live = 0;
   if (threadIdx.x < kMTile) {
     const int m = threadIdx.x;
     int4 row = make_int4(-1, 0, 0, -1);
@@ -178,10 +182,9 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
       }
     }
     s_rows[m] = row;
-    live = row.x >= 0;
   }
   tc_fence_before_sync();
-  const int n_live = __syncthreads_count(live);
+  __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t tmem_a = tmem_base + kAccCols;  // A operand columns
@@ -212,14 +215,21 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
         *abort_flag = 1;
         break;
       }
-      const uint32_t ubytes = static_cast<uint32_t>(min(kTileN, p.V - v0)) * 4u;
-      if (lane == 0) mbar_arrive_expect_tx(bar_ufull + 8 * s, ubytes * static_cast<uint32_t>(n_live));
+      // rows 4g .. 4g+3 by lane g (idle rows read U row 0; the box counts in
+      // full, columns past V zero-filled)
+      const int ngroups = (rows_valid + 3) >> 2;
+      if (lane == 0) mbar_arrive_expect_tx(bar_ufull + 8 * s, static_cast<uint32_t>(ngroups) * 4u * kResURow);
       __syncwarp();
-      for (int m = lane; m < rows_valid; m += 32) {
-        const int4 row = s_rows[m];
-        if (row.x < 0) continue;
-        const size_t urow = static_cast<size_t>(row.y) * p.gamma + row.z;
-        bulk_load(base + plan.u(s) + m * kUStride, p.U + urow * p.V + v0, ubytes, bar_ufull + 8 * s, pol_u);
+      if (lane < ngroups) {
+        int rc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int m = 4 * lane + k;
+          const int4 row = m < rows_valid ? s_rows[m] : make_int4(-1, 0, 0, -1);
+          rc[k] = row.x >= 0 ? row.y * p.gamma + row.z : 0;
+        }
+        tma_gather4(base + plan.u(s) + lane * 4 * kResURow, &tm_u, bar_ufull + 8 * s, v0, rc[0], rc[1], rc[2], rc[3],
+                    pol_u);
       }
       __syncwarp();
       ++filled;
@@ -358,7 +368,7 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
         break;
       }
       float u[32];
-      const float4* urow = reinterpret_cast<const float4*>(gbase + plan.u(s) + row * kUStride + h * 128);
+      const float4* urow = reinterpret_cast<const float4*>(gbase + plan.u(s) + row * kResURow + h * 128);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const float4 t4 = urow[k];

@@ -457,7 +457,8 @@ __global__ void __launch_bounds__(256) k4_c_star(const VerifyArgs p) {
 
 // The residual pass of verify, chained to the accept kernel with programmatic
 // dependent launch.
-static cudaError_t launch_residual_partials(const CUtensorMap& tm_w2, const ResidualArgs& a, cudaStream_t stream) {
+static cudaError_t launch_residual_partials(const CUtensorMap& tm_w2, const CUtensorMap& tm_u, const ResidualArgs& a,
+                                            cudaStream_t stream) {
   const ResidualSmem plan = residual_smem_plan(a.rank);
   const dim3 grid(a.grid);
   static std::once_flag once;
@@ -465,7 +466,7 @@ static cudaError_t launch_residual_partials(const CUtensorMap& tm_w2, const Resi
     cudaFuncSetAttribute(k_residual_partials, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(residual_smem_plan(256).total));
   });
-  return launch_pdl(k_residual_partials, grid, dim3(kDraftThreads), plan.total, stream, true, tm_w2, a);
+  return launch_pdl(k_residual_partials, grid, dim3(kDraftThreads), plan.total, stream, true, tm_w2, tm_u, a);
 }
 
 int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors,
@@ -530,9 +531,10 @@ int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint
   a.R = R; a.R_pad = p.R_pad; a.gamma = gamma; a.V = V; a.rank = rank;
   a.n_tiles = p.n_tiles; a.grid = p.res_grid;
   a.scale = p.scale;
-  CUtensorMap tm_w2;
-  if (encode_w2_map(&tm_w2, W2, V, rank) != DSPARK_OK) return DSPARK_ERR_CUDA;
-  if (launch_residual_partials(tm_w2, a, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  CUtensorMap tm_w2, tm_u;
+  if (encode_w2_map(&tm_w2, W2, V, rank) != DSPARK_OK || encode_u_rows_map(&tm_u, U, R, gamma, V) != DSPARK_OK)
+    return DSPARK_ERR_CUDA;
+  if (launch_residual_partials(tm_w2, tm_u, a, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   if (p.all_rows &&
       launch_pdl(k4_c_star, dim3(ceil_div(R * gamma, 8)), dim3(256), 0, stream, true, p) != cudaSuccess)
     return DSPARK_ERR_CUDA;

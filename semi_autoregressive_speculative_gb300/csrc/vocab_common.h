@@ -19,6 +19,10 @@ int encode_w2_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank);
 // W2 again, box 32 x rank without swizzle: the 32 columns of one sub-tile as
 // [rank][32] (the samplers' recompute of a sub-tile's bias).
 int encode_w2_slab_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank);
+// U [R, gamma, V] fp32 as a 2-D tensor of R * gamma rows (row = request *
+// gamma + position), box 64 x 1, no swizzle: rows gathered four at a time
+// (tile::gather4) by the verify residual pass.
+int encode_u_rows_map(CUtensorMap* tm, const float* U, int R, int gamma, int V);
 // Contiguous V-chunks per M-tile so that chunks x M-tiles fills the SMs once.
 int vocab_chunks(int n_tiles, int n_mtiles);
 
