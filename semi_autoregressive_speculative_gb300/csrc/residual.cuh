@@ -111,8 +111,11 @@ __global__ void __launch_bounds__(kDraftThreads, 1)
   if (static_cast<int>(blockIdx.x) >= n_mt * n_chunks) return;  // no work for this CTA
   const int mtile = blockIdx.x % n_mt;
   const int chunk = blockIdx.x / n_mt;
-  const int r0 = mtile * kMTile;
-  const int rows_valid = min(kMTile, nrows - r0);
+  // the rows are spread evenly over the M-tiles (a CTA's time grows with its
+  // live rows), M-tile k holding rows [k * rpt, (k + 1) * rpt)
+  const int rpt = (nrows + n_mt - 1) / n_mt;
+  const int r0 = mtile * rpt;
+  const int rows_valid = min(rpt, nrows - r0);
   const int t_begin = static_cast<int>((static_cast<long long>(chunk) * p.n_tiles) / n_chunks);
   const int t_end = static_cast<int>((static_cast<long long>(chunk + 1) * p.n_tiles) / n_chunks);
   const int ntile = t_end - t_begin;
