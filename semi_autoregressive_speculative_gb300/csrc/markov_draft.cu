@@ -7,13 +7,12 @@
 //            operand, once the samplers of the M-tile have published the
 //            previous tokens (a per-M-tile counter; the publishing sampler
 //            has already staged the row in gather order)
-//   tiles    W2 in 64-row K-chunks (L2-resident after the first position)
-//            and U tiles (one 128-row x 68-column box per tile: 272
-//            contiguous bytes per row, which is what lets the HBM stream run
-//            near its peak) come in through TMA rings, each fed by its own
-//            producer warp; tcgen05.mma into fp32 accumulators in tensor
-//            memory, two 64-column tiles per instruction (below); the
-//            epilogue takes a pair of tiles per iteration, adds U, scales by
+//   tiles    W2 in 128-row K-chunks (L2-resident after the first position)
+//            and U tiles (128 rows x 64 columns) come in through TMA rings,
+//            each fed by its own producer warp; U is copied into the fp32
+//            accumulators in tensor memory and tcgen05.mma adds the bias on
+//            top, two 64-column tiles per instruction (below); the epilogue
+//            takes a pair of tiles per iteration, scales z = U + bias by
 //            log2(e)/T and reduces each 32-column sub-tile and the whole
 //            chunk to softmax partials (max, sum exp2) — (max, argmax) when
 //            greedy.  Logits never reach HBM.  Each row's chunk partial is
@@ -48,17 +47,19 @@
 
 namespace dspark {
 
-// Tiles are multiplied in pairs.  An M=128, K=16 tcgen05.mma costs about the
-// same time at N=64 as at N=128 (about 100 cycles: the tensor pipe is bound
-// by the instruction, not by its N), so one N=128 instruction per K-step
-// covers two 64-column tiles and halves the tensor time per tile.
-// W2 comes in K-chunks: a ring stage holds 64 rank rows of both tiles of a
-// pair (two 64 x 64 boxes, 128-byte swizzled, 8 KB apart: the B descriptor
+// Tiles are multiplied in pairs.  An M=128, K=16 tcgen05.mma costs about 66
+// cycles at N=64 and 80 at N=128 (microbenchmark, one CTA), so one N=128
+// instruction per K-step covers two 64-column tiles at 0.62 cycles per column
+// against 1.03.
+// W2 comes in K-chunks: a ring stage holds 128 rank rows of both tiles of a
+// pair (two 128 x 64 boxes, 128-byte swizzled, 16 KB apart: the B descriptor
 // spans them as two swizzle atoms along N).  A stage is released as soon as
-// its 4 MMAs are done, so the ring keeps most of its bytes in flight.
-constexpr int kDraftKChunk = 64;     // rank rows per W2 stage
+// its 8 MMAs are done.  The issuing thread pays for every wait and commit
+// (about 110 and 220 cycles: 16 MMAs cost 1 430 cycles back to back and 2 770
+// with a wait and a commit every 4), so a pair takes two chunks, not four.
+constexpr int kDraftKChunk = 128;    // rank rows per W2 stage (fewer, when the rank is smaller)
 constexpr int kDraftWBox = kDraftKChunk * 128;  // bytes of one 64-column box of a stage
-constexpr int kDraftWStages = 8;     // W2 K-chunk stages (L2-resident after the first position)
+constexpr int kDraftWStages = 4;     // W2 K-chunk stages (L2-resident after the first position)
 constexpr int kDraftUStages = 2;     // U tiles staged in shared memory (tensor memory holds 3 pairs more)
 constexpr int kDraftAccPairs = 3;    // fp32 accumulator pairs (2 x 64 columns each) in tensor memory
 constexpr int kDraftACol = kDraftAccPairs * 2 * kTileN;  // first tensor-memory column of the A operand
@@ -108,7 +109,9 @@ enum TraceEvent {
   kEvReadySeen = 11,  // the previous position's tokens of the M-tile are all published
   kEvCopyFirst = 12,  // copier: the position's first pair of U is in tensor memory (issued)
   kEvCopyThird = 13,  // copier: the position's third pair of U is in tensor memory (issued)
-  kTraceEvents = 14
+  kEvStart = 14,      // the CTA's set-up is done (position 0's slot only)
+  kEvEnd = 15,        // the CTA is about to free its tensor memory and exit (position 0's slot only)
+  kTraceEvents = 16
 };
 #ifdef DSPARK_DRAFT_TRACE
 #define DRAFT_TRACE(p, step, ev)                                                                         \
@@ -156,7 +159,7 @@ struct DraftSmem {
 __host__ __device__ inline DraftSmem draft_smem_plan(int rank) {
   DraftSmem s;
   uint32_t off = 0;
-  s.w0 = off; s.wstride = 2u * kDraftWBox; off += kDraftWStages * s.wstride;  // 2 x (64 rows x 64 bf16), SW128
+  s.w0 = off; s.wstride = 2u * kDraftWBox; off += kDraftWStages * s.wstride;  // 2 x (128 rows x 64 bf16), SW128
   s.u0 = off; off += kDraftUStages * kDraftUBytes;
   s.half = off; off += kMTile * 8;
   s.bars = off; off += 320;
@@ -819,11 +822,17 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t tmem_a = tmem_base + kDraftACol;  // A operand columns
+  if (threadIdx.x == 0) DRAFT_TRACE(p, 0, kEvStart);
   // tile i of a position belongs to pair i / 2; pair gp of the call uses
   // accumulator pair gp % kDraftAccPairs and W2 K-chunks g = gp * nkc + kc,
   // in ring stage g % kDraftWStages
   const int npair = (ntile + 1) >> 1;
-  const int nkc = p.rank / kDraftKChunk;
+  // W2 K-chunks of a pair: kc_rows rank rows each (the TMA box height), the
+  // last one partial when the rank is not a multiple of it (rows past the
+  // rank are zero-filled and skipped by the MMA)
+  const int kc_rows = min(kDraftKChunk, p.rank);
+  const int nkc = (p.rank + kc_rows - 1) / kc_rows;
+  const uint32_t w_box = static_cast<uint32_t>(kc_rows) * 128u;  // bytes of one 64-column box
 
   if (warp == 0) {
     // ---------------------------------------------------------- W2 producer (all positions, lane 0)
@@ -846,10 +855,11 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
               ok = false;
               break;
             }
-            // rows [kc * 64, kc * 64 + 64) of both tiles; columns past V are zero-filled
-            mbar_arrive_expect_tx(bar_wfull + 8 * sw, (two ? 2u : 1u) * kDraftWBox);
-            tma_load_2d(base + plan.w(sw), &tm_w2, bar_wfull + 8 * sw, va, kc * kDraftKChunk, pol_w);
-            if (two) tma_load_2d(base + plan.w(sw) + kDraftWBox, &tm_w2, bar_wfull + 8 * sw, vb, kc * kDraftKChunk, pol_w);
+            // rank rows [kc * kc_rows, (kc + 1) * kc_rows) of both tiles; rows past the
+            // rank and columns past V are zero-filled
+            mbar_arrive_expect_tx(bar_wfull + 8 * sw, (two ? 2u : 1u) * w_box);
+            tma_load_2d(base + plan.w(sw), &tm_w2, bar_wfull + 8 * sw, va, kc * kc_rows, pol_w);
+            if (two) tma_load_2d(base + plan.w(sw) + w_box, &tm_w2, bar_wfull + 8 * sw, vb, kc * kc_rows, pol_w);
             wlast = (wlast & ~(3u << (2 * sw))) | ((1u | (par << 1)) << (2 * sw));
           }
         }
@@ -971,13 +981,14 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
               break;
             }
             tc_fence_after_sync();
+            // K-steps of 16 rank rows in this chunk; N-direction atom stride
+            // (LBO) = one box: the pair's second tile
+            const int ks0 = kc * (kc_rows / 16), nks = min(kc_rows, p.rank - kc * kc_rows) / 16;
+            const uint64_t desc0 = smem_desc_sw128(base + plan.w(sw), w_box, 1024);
 #pragma unroll
-            for (int q4 = 0; q4 < kDraftKChunk / 16; ++q4) {
-              // N-direction atom stride (LBO) = one box: the pair's second tile
-              const uint32_t b_addr = base + plan.w(sw) + q4 * 2048;
-              const int ks = kc * (kDraftKChunk / 16) + q4;
-              umma_bf16_ts(d, tmem_a + ks * 8, smem_desc_sw128(b_addr, kDraftWBox, 1024), idesc, 1u);  // onto U
-            }
+            for (int q4 = 0; q4 < kDraftKChunk / 16; ++q4)
+              if (q4 < nks)  // + q4 * 2048 bytes: 16 rows of 128 bytes
+                umma_bf16_ts(d, tmem_a + (ks0 + q4) * 8, desc0 + static_cast<uint64_t>(q4 * 128), idesc, 1u);  // onto U
             umma_commit(bar_wempty + 8 * sw);
             issued = 1;
           }
@@ -1198,6 +1209,7 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
   if (*abort_flag && threadIdx.x == 0) report(p.status, DSPARK_STATUS_TIMEOUT);
   tc_fence_before_sync();
   __syncthreads();
+  if (threadIdx.x == 0) DRAFT_TRACE(p, 0, kEvEnd);
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kDraftTmemCols);
@@ -1233,14 +1245,15 @@ int encode_w2_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank) {
   return rc == CUDA_SUCCESS ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
-// W2 [rank, V] bf16, box 64 x 64 with 128-byte swizzle: one K-chunk of one
-// tile of the draft's W2 ring (the MN-major SW128 operand layout of the UMMA).
+// W2 [rank, V] bf16, box 64 columns x min(128, rank) rows with 128-byte
+// swizzle: one K-chunk of one tile of the draft's W2 ring (the MN-major SW128
+// operand layout of the UMMA).
 static int encode_w2_kchunk_map(CUtensorMap* tm, const uint16_t* W2, int V, int rank) {
   auto fn = get_encode_fn();
   if (!fn) return DSPARK_ERR_CUDA;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(rank)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), static_cast<cuuint32_t>(kDraftKChunk)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), static_cast<cuuint32_t>(std::min(kDraftKChunk, rank))};
   cuuint32_t estr[2] = {1, 1};
   const CUresult rc = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W2), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -1,7 +1,7 @@
 """Per-position phase breakdown of the Markov draft kernel (a profiling tool).
 
     python -m semi_autoregressive_speculative_gb300.draft_trace \\
-        [--workload r128_g16_v151936] [--temperature 1.0] [--calls 5]
+        [--workload r128_g16_v151936] [--temperature 1.0] [--calls 5] [--lib PATH]
 
 Builds ``lib/libdspark_trace.so`` (build.py --trace: the same sources with the
 draft kernel's global-timer stamps compiled in), runs dspark_markov_draft on the
@@ -23,12 +23,12 @@ from . import build as pkg_build
 from . import synth
 
 EVENTS = ["a_ready", "first_acc", "tiles_done", "entry", "poll_done", "chunk_found", "fine_loaded", "slab_issued",
-          "slab_landed", "picked", "published", "ready_seen", "copy_first", "copy_third"]
+          "slab_landed", "picked", "published", "ready_seen", "copy_first", "copy_third", "start", "end"]
 K_MTILE, K_TILE_N, K_MAX_CHUNKS = 128, 64, 1024
 
 
-def _lib():
-    L = ctypes.CDLL(pkg_build.build(trace=True))
+def _lib(path=None):
+    L = ctypes.CDLL(path or pkg_build.build(trace=True))
     P, I, F, U64, U32, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32,
                              ctypes.c_size_t)
     L.dspark_workspace_size.restype = SZ
@@ -80,6 +80,13 @@ def phases(tr: np.ndarray, R: int) -> dict:
         "next_copy_first_after_tiles": us([e["copy_first"][j + 1] - e["tiles_done"][j] for j in js]),
         "next_copy_third_after_tiles": us([e["copy_third"][j + 1] - e["tiles_done"][j] for j in js]),
     }
+    # the call outside the position periods: set-up to position 0's A operand, and the last position's
+    # publish to the last CTA's exit
+    start, end = e["start"][0], e["end"][0]
+    out["kernel_span"] = float(end.max() - start.min()) / 1e3
+    out["setup_to_first_a"] = us(e["a_ready"][0] - start.min())
+    out["first_position_period"] = us(e["a_ready"][1] - e["a_ready"][0])
+    out["last_position_a_to_end"] = float(end.max() - np.median(e["a_ready"][g - 1])) / 1e3
     return out
 
 
@@ -89,10 +96,11 @@ def main(argv=None):
     ap.add_argument("--workload", default="r128_g16_v151936")
     ap.add_argument("--temperature", type=float, default=None)
     ap.add_argument("--calls", type=int, default=5)
+    ap.add_argument("--lib", default=None, help="a library built with the trace stamps (default: build lib/libdspark_trace.so)")
     args = ap.parse_args(argv)
     wl = synth.WORKLOADS[args.workload]
     temp = wl.temperatures[0] if args.temperature is None else args.temperature
-    L = _lib()
+    L = _lib(args.lib)
     dev = torch.device("cuda", 0)
     W1, W2, _ = synth.weights(wl)
     inp = synth.round_inputs(wl, 0)
