@@ -76,3 +76,69 @@ def test_noalloc_matches_workspace_draft_two_calls_in_a_row(name, R, gamma, V, t
             torch.cuda.synchronize()
             _compare(dr, ref, tok, pd, lz)
             assert int(status.item()) == 0
+
+
+def _noalloc_outputs(dr):
+    return torch.empty_like(dr.tokens), torch.empty_like(dr.pd), torch.empty_like(dr.logZ)
+
+
+@pytest.mark.gpu
+def test_noalloc_large_shape_then_small_shape():
+    """The shared scratch keeps a larger call's partials and sync words; a
+    smaller call after it must not read any of them."""
+    from semi_autoregressive_speculative_gb300 import dspark_markov_draft_noalloc
+    base = synth.WORKLOADS["r128_g16_v151936"]
+    shapes = [("large", 256, 2, 129280, 1.0), ("small", 5, 4, 4104, 1.0), ("small_greedy", 130, 3, 8200, 0.0)]
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    for name, R, gamma, V, temperature in shapes:
+        wl = synth.scaled(base, R=R, gamma=gamma, V=V, d=16, name="noalloc_seq_" + name)
+        dr, _ = device_round(wl)
+        dr.draft(temperature, wl.seed, 0)
+        ref = (host(dr.tokens).copy(), host(dr.pd).copy(), host(dr.logZ).copy())
+        assert dr.status() == 0
+        tok, pd, lz = _noalloc_outputs(dr)
+        dspark_markov_draft_noalloc(dr.U, dr.W1, dr.W2, dr.anchors, temperature, wl.seed, 0, tok, pd, lz,
+                                    status=status)
+        torch.cuda.synchronize()
+        _compare(dr, ref, tok, pd, lz)
+        assert int(status.item()) == 0
+        del dr
+        torch.cuda.empty_cache()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("temperature", [1.0, 0.0])
+def test_noalloc_captured_in_a_graph_after_warm_up(temperature):
+    """The use the header names: one eager call, then the call recorded into a
+    CUDA graph and replayed on new U (written into the same buffer), each replay
+    checked against the workspace entry point on that round's inputs."""
+    from semi_autoregressive_speculative_gb300 import dspark_markov_draft_noalloc
+    wl = synth.scaled(synth.WORKLOADS["r128_g16_v151936"], R=130, gamma=3, V=8200, d=16, name="noalloc_graph")
+    dr, _ = device_round(wl)
+    tok, pd, lz = _noalloc_outputs(dr)
+    status = torch.full((1,), -1, dtype=torch.int32, device=dr.device)
+    rnd = 0
+    dspark_markov_draft_noalloc(dr.U, dr.W1, dr.W2, dr.anchors, temperature, wl.seed, rnd, tok, pd, lz, status=status)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=side):
+        dspark_markov_draft_noalloc(dr.U, dr.W1, dr.W2, dr.anchors, temperature, wl.seed, rnd, tok, pd, lz,
+                                    status=status)
+    torch.cuda.synchronize()
+    for k in range(3):
+        # a new round's U in the captured buffer (same seed and round: only U differs)
+        inp = synth.round_inputs(wl, k + 1)
+        dr.U.copy_(torch.from_numpy(inp.U))
+        dr.draft(temperature, wl.seed, rnd)
+        ref = (host(dr.tokens).copy(), host(dr.pd).copy(), host(dr.logZ).copy())
+        assert dr.status() == 0
+        tok.fill_(-7)
+        pd.fill_(-1.0)
+        lz.fill_(float("nan"))
+        status.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        _compare(dr, ref, tok, pd, lz)
+        assert int(status.item()) == 0
