@@ -110,6 +110,31 @@ int dspark_markov_draft(const float *U, const uint16_t *W1, const uint16_t *W2,
                         void *stream);
 
 /*
+ * The same draft with the LM head fused in: the pre-LM-head hidden states h
+ * are given instead of the logits U, and U = h . W_lm is formed tile by tile
+ * inside the draft (hidden-state communication: "DSpark: Speculative
+ * decodingを活用した…", "実サービス配備 › 拡張可能な学習 › 隠れ状態通信" ships the
+ * hidden state rather than V-wide logits and runs the LM head where the
+ * tokens are drawn).  For each request r and position j:
+ *     z_j(v) = (h[r,j,:] . W_lm[:,v] + W1[x_{j-1}] . W2[:,v]) / T
+ * and the rest exactly as dspark_markov_draft (same outputs, same sampling,
+ * same Philox draws).  Both dot products accumulate in one fp32 sum of bf16
+ * products (tensor cores), so U is never rounded to fp32 on its own.
+ *   h        bf16 [R, gamma, d]   pre-LM-head hidden states (16-byte aligned)
+ *   W_lm     bf16 [d, V]          LM-head weight (16-byte aligned)
+ *   W1, W2, anchors, tokens, pd_tok, logZ, workspace   as for dspark_markov_draft
+ * Sizes: as dspark_markov_draft, and d % 128 == 0, d <= 65536.
+ * Cost: W_lm is read once per position (gamma * d * V * 2 bytes a call), so at
+ * batch sizes where R * gamma * V * 4 < gamma * d * V * 2 (R < d / 2) reading a
+ * materialised U through dspark_markov_draft moves fewer bytes.
+ */
+int dspark_markov_draft_lmhead(const uint16_t *h, const uint16_t *W_lm, const uint16_t *W1,
+                               const uint16_t *W2, const int32_t *anchors, int R, int gamma,
+                               int V, int rank, int d, float temperature, uint64_t seed,
+                               uint32_t round, int32_t *tokens, float *pd_tok, float *logZ,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Confidence head and survival products ("DSpark" §3.1 eq. c_k; §1.1 eq. a_j):
  *     c[r,j] = sigma( sum_i w[i] h[r,j,i] + sum_i w[d+i] W1[x_{j-1}, i] ),  x_{-1} = anchor
  *     a[r,j] = fp32(a[r,j-1] * c[r,j]),  a[r,-1] = 1  (left to right)

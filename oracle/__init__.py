@@ -101,6 +101,31 @@ def uniform(seed: int, rnd: int, request: int, position: int, purpose: int) -> f
 
 
 # ---------------------------------------------------------------- draft
+def _bf16_f64(bits) -> np.ndarray:
+    """bf16 bit patterns -> their exact values as fp64."""
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def lm_head_logits(h, W_lm, cols_per_block: int = 16384) -> np.ndarray:
+    """U = h . W_lm, the logits the fused LM-head draft forms from the shipped
+    pre-LM-head hidden state ("DSpark: Speculative decodingを活用した…",
+    "実サービス配備 › 拡張可能な学習 › 隠れ状態通信": the hidden state, not the
+    V-wide logits, crosses the wire and the LM head runs where the tokens are
+    drawn).  The bf16 values are multiplied and summed in fp64 (numpy's
+    matmul) and each sum is rounded once to fp32.  h bf16 bits [..., d], W_lm
+    bf16 bits [d, V] -> fp32 [..., V]; W_lm is decoded in blocks of columns to
+    bound the host memory."""
+    hf = _bf16_f64(h)
+    W_lm = np.asarray(W_lm, np.uint16)
+    d, V = W_lm.shape
+    assert hf.shape[-1] == d
+    out = np.empty(hf.shape[:-1] + (V,), np.float32)
+    for v0 in range(0, V, cols_per_block):
+        v1 = min(V, v0 + cols_per_block)
+        out[..., v0:v1] = (hf @ _bf16_f64(W_lm[:, v0:v1])).astype(np.float32)
+    return out
+
+
 def markov_bias(W1: np.ndarray, W2: np.ndarray, prev: int) -> np.ndarray:
     W1 = _c(W1, np.uint16)
     W2 = _c(W2, np.uint16)

@@ -26,7 +26,8 @@ DSPARK_STATUS_BAD_LENGTH = 8
 MODE_EARLY_STOP, MODE_TOP_K, MODE_FIXED = 0, 1, 2
 
 EXPORTS = ("dspark_workspace_size", "dspark_clear_status", "dspark_markov_draft", "dspark_confidence",
-           "dspark_schedule", "dspark_verify", "dspark_markov_draft_noalloc", "dspark_selftest_bounded_wait")
+           "dspark_schedule", "dspark_verify", "dspark_markov_draft_noalloc", "dspark_selftest_bounded_wait",
+           "dspark_markov_draft_lmhead")
 
 _lib = None
 
@@ -57,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.dspark_selftest_bounded_wait.argtypes = [P, P]
         L.dspark_markov_draft.restype = I
         L.dspark_markov_draft.argtypes = [P, P, P, P, I, I, I, I, F, U64, U32, P, P, P, P, SZ, P]
+        L.dspark_markov_draft_lmhead.restype = I
+        L.dspark_markov_draft_lmhead.argtypes = [P, P, P, P, P, I, I, I, I, I, F, U64, U32, P, P, P, P, SZ, P]
         L.dspark_confidence.restype = I
         L.dspark_confidence.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, SZ, P]
         L.dspark_schedule.restype = I
@@ -122,6 +125,18 @@ def dspark_markov_draft(U, W1, W2, anchors, temperature, seed, round_, tokens, p
         _ptr(U), _ptr(W1), _ptr(W2), _ptr(anchors), R, gamma, V, rank, float(temperature), int(seed),
         int(round_), _ptr(tokens), _ptr(pd_tok), _ptr(logZ), _ptr(workspace), _nbytes(workspace),
         _stream(stream)))
+
+
+def dspark_markov_draft_lmhead(h, W_lm, W1, W2, anchors, temperature, seed, round_, tokens, pd_tok, logZ, workspace,
+                               stream=None) -> None:
+    """The draft with the LM head fused in: h [R, gamma, d] bf16 and W_lm
+    [d, V] bf16 in place of U (see include/dspark.h)."""
+    R, gamma, d = h.shape
+    V = W_lm.shape[1]
+    rank = W1.shape[1]
+    _check("dspark_markov_draft_lmhead", lib().dspark_markov_draft_lmhead(
+        _ptr(h), _ptr(W_lm), _ptr(W1), _ptr(W2), _ptr(anchors), R, gamma, V, rank, d, float(temperature), int(seed),
+        int(round_), _ptr(tokens), _ptr(pd_tok), _ptr(logZ), _ptr(workspace), _nbytes(workspace), _stream(stream)))
 
 
 def dspark_confidence(h, W1, w, anchors, tokens, c, a, workspace, stream=None, sts_temperature=None) -> None:

@@ -11,6 +11,10 @@ namespace dspark {
 int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors, int R,
                         int gamma, int V, int rank, float temperature, uint64_t seed, uint32_t round,
                         int32_t* tokens, float* pd_tok, float* logZ, void* workspace, cudaStream_t stream);
+int launch_markov_draft_lmhead(const uint16_t* h, const uint16_t* W_lm, int d, const uint16_t* W1, const uint16_t* W2,
+                               const int32_t* anchors, int R, int gamma, int V, int rank, float temperature,
+                               uint64_t seed, uint32_t round, int32_t* tokens, float* pd_tok, float* logZ,
+                               void* workspace, cudaStream_t stream);
 int launch_confidence(const uint16_t* h, const uint16_t* W1, const float* w, const float* sts_t,
                       const int32_t* anchors, const int32_t* tokens, int R, int gamma, int d, int rank, int V,
                       float* c, float* a, int32_t* status, cudaStream_t stream);
@@ -69,6 +73,23 @@ int dspark_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
   if (workspace_bytes < workspace_layout(R, gamma, V).total) return DSPARK_ERR_INVALID_ARG;
   return launch_markov_draft(U, W1, W2, anchors, R, gamma, V, rank, temperature, seed, round, tokens, pd_tok, logZ,
                              workspace, static_cast<cudaStream_t>(stream));
+}
+
+int dspark_markov_draft_lmhead(const uint16_t* h, const uint16_t* W_lm, const uint16_t* W1, const uint16_t* W2,
+                               const int32_t* anchors, int R, int gamma, int V, int rank, int d, float temperature,
+                               uint64_t seed, uint32_t round, int32_t* tokens, float* pd_tok, float* logZ,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (R < 0 || gamma < 1 || V < 8 || rank < 1 || d < 1 || !finite_nonneg(temperature)) return DSPARK_ERR_INVALID_ARG;
+  if (gamma > kMaxGamma || V % 8 != 0 || !rank_ok(rank) || d % 128 != 0 || d > kMaxLmHeadD)
+    return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (R == 0) return DSPARK_OK;
+  if (!h || !W_lm || !W1 || !W2 || !anchors || !tokens || !pd_tok || !logZ || !workspace) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(W_lm) || !aligned16(W1) || !aligned16(W2) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return DSPARK_ERR_INVALID_ARG;
+  if (workspace_bytes < workspace_layout(R, gamma, V).total) return DSPARK_ERR_INVALID_ARG;
+  return launch_markov_draft_lmhead(h, W_lm, d, W1, W2, anchors, R, gamma, V, rank, temperature, seed, round, tokens,
+                                    pd_tok, logZ, workspace, static_cast<cudaStream_t>(stream));
 }
 
 int dspark_confidence(const uint16_t* h, const uint16_t* W1, const float* w, const float* sts_temperature,

@@ -21,6 +21,7 @@ constexpr int kPfTiles = 4;        // tiles per L2 prefetch group (a 256-column 
 constexpr int kDraftThreads = 320; // warp 0 TMA producer, warp 1 MMA, warps 2..9 epilogue
 constexpr int kVerifyChunk = 1024; // target columns per verify statistics item (32 per lane)
 constexpr int kMaxGamma = 64;
+constexpr int kMaxLmHeadD = 65536;  // hidden size bound of the fused LM-head draft
 constexpr int kMaxSchedule = 8192; // R * gamma handled by the one-CTA scheduler
 constexpr int kMaxVerifyR = 32768; // verify keeps R + 1 row offsets in shared memory
 

@@ -126,7 +126,8 @@ enum TraceEvent {
 #endif
 
 struct DraftArgs {
-  const float* U;          // [R, gamma, V]
+  const float* U;          // [R, gamma, V] (null with the LM head)
+  const uint16_t* h;       // [R, gamma, d] bf16 pre-LM-head hidden states (LM head only)
   const uint16_t* W1;      // [V, rank]
   const uint16_t* W2;      // [rank, V]
   const int32_t* anchors;  // [R]
@@ -143,6 +144,7 @@ struct DraftArgs {
   unsigned long long* trace;  // [gamma][n_ctas][kTraceEvents] or null
 #endif
   int R, R_pad, gamma, V, rank, n_tiles, n_chunks, n_mtiles;
+  int d;                   // hidden size (LM head only; 0 otherwise)
   float scale;             // log2(e) / T (1 when greedy)
   uint64_t seed;
   uint32_t round;
@@ -168,7 +170,7 @@ __host__ __device__ inline DraftSmem draft_smem_plan(int rank) {
   s.wts = off; off += kMaxSampleChunks * 4;      // the leader's search weights
   s.ev = off; off += 256 * 4;                    // the previous token's W1 row
   off = (off + 127u) & ~127u;
-  s.slab = off; off += 64u * rank + 32 * 4;      // W2 columns [rank][32] bf16, then 32 U values
+  s.slab = off; off += (rank > 256 ? 64u * rank : 64u * 256u) + 32 * 4;  // [<=256][32] bf16 columns, then 32 U values
   s.total = off + 1024;  // alignment slack
   return s;
 }
@@ -518,8 +520,9 @@ struct SampleSmem {
   SampleSlot* slot;
   float* part;      // [8 warps][32 columns] shares of the bias
   float* wts;       // [kMaxSampleChunks] search weights of the leader
-  float* ev;        // [256] the previous token's W1 row (fp32)
-  uint8_t* slab;    // [rank][32] bf16: W2 columns of the chosen sub-tile, then U of the sub-tile (32 fp32)
+  float* ev;        // [256] the previous token's W1 row (fp32); with the LM head, then a chunk of h
+  uint8_t* slab;    // [rank][32] bf16: W2 columns of the chosen sub-tile, then U of the sub-tile (32 fp32);
+                    // with the LM head, then [256][32] chunks of W_lm's columns
   uint32_t slab_s;  // shared-space address of `slab`
   uint32_t bar;     // mbarrier of the slab copies
 };
@@ -533,13 +536,18 @@ struct SampleSmem {
 // shared memory), and copies that sub-tile's W2 columns (one TMA box,
 // rank x 32) and U values (one bulk copy) into shared memory.  Each warp then
 // sums its 32 rank rows for the 32 columns (a lane per column), and the leader
-// adds the shares and U and picks the token.  Returns the number of slab copies
-// waited for (0 or 1: add it to `phase`), or -1 (the same in every warp: it
-// follows the slot, read after a barrier) when the leader's wait gave up.  The
-// arguments are plain values so that nothing of the sampler lives in local
-// memory.
-__device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap* tm_slab, int r, int step, int sub,
-                                       const SampleSmem sm, const uint32_t phase, volatile int* abort_flag) {
+// adds the shares and U and picks the token.  With the LM head (kLm) there is
+// no U to copy: the warps add h . W_lm of the 32 columns instead, from
+// 256-row chunks of W_lm's columns copied into the slab one after another
+// (each thread stages one value of the row's h per chunk).  Returns the number
+// of slab copies waited for (add it to `phase`), or -1 (the same in every
+// warp: it follows the slot, read after a barrier) when the leader's wait gave
+// up.  The arguments are plain values so that nothing of the sampler lives in
+// local memory.
+template <bool kLm>
+__device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap* tm_slab,
+                                          const CUtensorMap* tm_lmslab, int r, int step, int sub,
+                                          const SampleSmem sm, const uint32_t phase, volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
   const size_t out = static_cast<size_t>(r) * p.gamma + step;
   SampleSlot& slot = *sm.slot;
@@ -615,10 +623,10 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
           fence_proxy_async_smem();
           // W2[:, v0 .. v0+31] (columns past V zero-filled) and U[r, step, v0 .. v0+31]
           const int v0 = sstar * kSubN;
-          const uint32_t ubytes = static_cast<uint32_t>(min(kSubN, p.V - v0)) * 4u;  // a multiple of 32
+          const uint32_t ubytes = kLm ? 0u : static_cast<uint32_t>(min(kSubN, p.V - v0)) * 4u;  // a multiple of 32
           mbar_arrive_expect_tx(sm.bar, static_cast<uint32_t>(p.rank) * 64u + ubytes);
           tma_load_2d(sm.slab_s, tm_slab, sm.bar, v0, 0, policy_evict_normal());
-          bulk_load(sm.slab_s + p.rank * 64, p.U + out * p.V + v0, ubytes, sm.bar, policy_evict_first());
+          if (!kLm) bulk_load(sm.slab_s + p.rank * 64, p.U + out * p.V + v0, ubytes, sm.bar, policy_evict_first());
           if (traced) DRAFT_TRACE(p, step, kEvSlabIssued);
         }
       }
@@ -644,12 +652,41 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
     // this warp's share of the 32 bias values: lane l sums column v0 + l over
     // the warp's rank rows (W1 entries read as shared-memory broadcasts)
     float acc = 0.f;
+    const uint16_t* slab = reinterpret_cast<const uint16_t*>(sm.slab);
     if (landed) {
-      const uint16_t* slab = reinterpret_cast<const uint16_t*>(sm.slab);
 #pragma unroll 8
       for (int k = 0; k < 32; ++k) {
         const int jk = sub * 32 + k;
         if (jk < p.rank) acc = fmaf(sm.ev[jk], __uint_as_float(static_cast<uint32_t>(slab[jk * 32 + lane]) << 16), acc);
+      }
+    }
+    if constexpr (kLm) {
+      // + h[r, step, :] . W_lm[:, v0 + lane], 256 rows of W_lm per copy
+      const int v0 = sstar * kSubN;
+      const int nlm = (p.d + 255) / 256;
+      for (int c = 0; c < nlm; ++c) {
+        named_barrier(5, kEpiThreads);  // every warp is done with the slab and ev of the previous copy
+        const int jt = sub * 32 + lane, jj = c * 256 + jt;
+        sm.ev[jt] = jj < p.d ? bf16_at(p.h + out * p.d + jj) : 0.f;
+        if (sub == 0 && lane == 0 && !*abort_flag) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(sm.bar, 256u * 64u);  // rows past d are zero-filled
+          tma_load_2d(sm.slab_s, tm_lmslab, sm.bar, v0, c * 256, policy_evict_first());
+        }
+        named_barrier(5, kEpiThreads);  // ev is written
+        const bool got = __all_sync(0xffffffffu, mbar_wait(sm.bar, (phase + 1u + static_cast<uint32_t>(c)) & 1u,
+                                                           abort_flag));
+        if (!got) {
+          *abort_flag = 1;
+          landed = false;
+        }
+        if (got) {
+#pragma unroll 8
+          for (int k = 0; k < 32; ++k) {
+            const int jk = sub * 32 + k;
+            acc = fmaf(sm.ev[jk], __uint_as_float(static_cast<uint32_t>(slab[jk * 32 + lane]) << 16), acc);
+          }
+        }
       }
     }
     sm.part[sub * 32 + lane] = acc;
@@ -677,7 +714,7 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
       const int v = v0 + lane;
       float y = -INFINITY, w = 0.f;
       if (v < p.V) {
-        y = (bias + reinterpret_cast<const float*>(sm.slab + p.rank * 64)[lane]) * p.scale;
+        y = (kLm ? bias : bias + reinterpret_cast<const float*>(sm.slab + p.rank * 64)[lane]) * p.scale;
         w = ex2(y - M);
       }
       const float incl = before_s + warp_incl_scan_f(w);
@@ -704,7 +741,7 @@ __device__ __forceinline__ int sample_cta(const DraftArgs& p, const CUtensorMap*
   // the slot, the shares and the slab are rewritten for the next request only
   // after that request's first barrier, which the leader reaches only after
   // it has finished reading them here
-  return state == kSlotAbort ? -1 : (state == kSlotSample ? 1 : 0);
+  return state == kSlotAbort ? -1 : (state == kSlotSample ? (kLm ? 1 + (p.d + 255) / 256 : 1) : 0);
 }
 
 // 5-D tiled tensor load (coordinates in elements, innermost first).
@@ -752,11 +789,16 @@ __device__ __forceinline__ void merge_partial(float mx, float sm, float& runM, f
   }
 }
 
-template <bool kGreedy>
+// kLm: the fused LM head.  U is not read: each pair's accumulators start from
+// h_j . W_lm, computed by the same MMAs over d more rank rows (A = h rows of
+// the M-tile by TMA through the U stages, B = W_lm K-chunks through the W2
+// ring), and then take the bias on top.  tm_u5 and tm_u3 are then the W_lm
+// K-chunk and h maps, and tm_lmslab the sampler's W_lm column map.
+template <bool kGreedy, bool kLm>
 __global__ void __launch_bounds__(kDraftKThreads, 1)
     k_markov_draft(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u5,
                    const __grid_constant__ CUtensorMap tm_u3, const __grid_constant__ CUtensorMap tm_slab,
-                   const DraftArgs p) {
+                   const __grid_constant__ CUtensorMap tm_lmslab, const DraftArgs p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -809,9 +851,10 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tm_w2);
-    if ((p.R & 7) == 0) prefetch_tensormap(&tm_u5);
+    if (kLm || (p.R & 7) == 0) prefetch_tensormap(&tm_u5);
     prefetch_tensormap(&tm_u3);
     prefetch_tensormap(&tm_slab);
+    if (kLm) prefetch_tensormap(&tm_lmslab);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kDraftTmemCols);
@@ -833,11 +876,16 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
   const int kc_rows = min(kDraftKChunk, p.rank);
   const int nkc = (p.rank + kc_rows - 1) / kc_rows;
   const uint32_t w_box = static_cast<uint32_t>(kc_rows) * 128u;  // bytes of one 64-column box
+  // with the LM head, a pair first takes nkl K-chunks of W_lm (d % 128 == 0),
+  // then the nkc of W2: nkw ring stages per pair in all
+  const int nkl = kLm ? p.d / kDraftKChunk : 0;
+  const int nkw = nkl + nkc;
 
   if (warp == 0) {
     // ---------------------------------------------------------- W2 producer (all positions, lane 0)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_last();
+      const uint64_t pol_lm = policy_evict_first();
       uint32_t wlast = 0;  // per stage s: bit 2s = filled, bit 2s + 1 = parity of its last fill
       bool ok = true;
       for (int step = 0; step < p.gamma && ok; ++step) {
@@ -846,8 +894,8 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
           const bool two = 2 * j + 1 < ntile;
           const int va = (t_begin + tile_of(step, 2 * j, ntile)) * kTileN;
           const int vb = two ? (t_begin + tile_of(step, 2 * j + 1, ntile)) * kTileN : 0;
-          for (int kc = 0; kc < nkc; ++kc) {
-            const int g = gp * nkc + kc;
+          for (int kc = 0; kc < nkw; ++kc) {
+            const int g = gp * nkw + kc;
             const int sw = g % kDraftWStages;
             const uint32_t par = static_cast<uint32_t>(g / kDraftWStages) & 1u;
             if (!mbar_wait(bar_wempty + 8 * sw, par ^ 1u, abort_flag)) {
@@ -855,11 +903,19 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
               ok = false;
               break;
             }
-            // rank rows [kc * kc_rows, (kc + 1) * kc_rows) of both tiles; rows past the
-            // rank and columns past V are zero-filled
-            mbar_arrive_expect_tx(bar_wfull + 8 * sw, (two ? 2u : 1u) * w_box);
-            tma_load_2d(base + plan.w(sw), &tm_w2, bar_wfull + 8 * sw, va, kc * kc_rows, pol_w);
-            if (two) tma_load_2d(base + plan.w(sw) + w_box, &tm_w2, bar_wfull + 8 * sw, vb, kc * kc_rows, pol_w);
+            if (kLm && kc < nkl) {
+              // W_lm rows [kc * 128, kc * 128 + 128) of both tiles (streamed: evict first)
+              mbar_arrive_expect_tx(bar_wfull + 8 * sw, (two ? 2u : 1u) * kDraftWBox);
+              tma_load_2d(base + plan.w(sw), &tm_u5, bar_wfull + 8 * sw, va, kc * kDraftKChunk, pol_lm);
+              if (two) tma_load_2d(base + plan.w(sw) + kDraftWBox, &tm_u5, bar_wfull + 8 * sw, vb, kc * kDraftKChunk, pol_lm);
+            } else {
+              // rank rows [kw * kc_rows, (kw + 1) * kc_rows) of both tiles; rows past the
+              // rank and columns past V are zero-filled
+              const int kw = kc - nkl;
+              mbar_arrive_expect_tx(bar_wfull + 8 * sw, (two ? 2u : 1u) * w_box);
+              tma_load_2d(base + plan.w(sw), &tm_w2, bar_wfull + 8 * sw, va, kw * kc_rows, pol_w);
+              if (two) tma_load_2d(base + plan.w(sw) + w_box, &tm_w2, bar_wfull + 8 * sw, vb, kw * kc_rows, pol_w);
+            }
             wlast = (wlast & ~(3u << (2 * sw))) | ((1u | (par << 1)) << (2 * sw));
           }
         }
@@ -874,6 +930,40 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
       }
     }
     __syncwarp();
+  } else if (kLm && warp == kUWarp) {
+    // ---------------------------------------------------------- h producer (LM head; all positions, lane 0)
+    // each LM K-chunk of a pair: the M-tile's h rows at this position, K
+    // elements [kc * 128, kc * 128 + 128) as two 64-element SW128 boxes (rows
+    // past R zero-filled), into a U stage
+    if (lane == 0) {
+      const uint64_t pol_h = policy_evict_last();  // reread by every pair of the position
+      int hfilled = 0;
+      for (int gp = 0; gp < npair * p.gamma && !*abort_flag; ++gp) {
+        const int step = gp / npair;
+        for (int kc = 0; kc < nkl; ++kc) {
+          const int gh = gp * nkl + kc, hs = gh % kDraftUStages;
+          if (!mbar_wait(bar_uempty + 8 * hs, ((gh / kDraftUStages) & 1) ^ 1, abort_flag)) {
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_ufull + 8 * hs, kDraftUBytes);
+          tma_load_3d(base + plan.u(hs), &tm_u3, bar_ufull + 8 * hs, kc * kDraftKChunk, step, r0, pol_h);
+          tma_load_3d(base + plan.u(hs) + kDraftUBytes / 2, &tm_u3, bar_ufull + 8 * hs, kc * kDraftKChunk + 64, step, r0,
+                      pol_h);
+          ++hfilled;
+        }
+      }
+      if (*abort_flag) {
+        const uint64_t t0 = global_ns();
+        for (int i = max(0, hfilled - kDraftUStages); i < hfilled; ++i)
+          while (!mbar_try_wait(bar_ufull + 8 * (i % kDraftUStages), (i / kDraftUStages) & 1) &&
+                 global_ns() - t0 < kWaitLimitNs) {
+          }
+      }
+    }
+    __syncwarp();
+  } else if (kLm && warp == kCopyWarp) {
+    // no U to copy: the MMA issuer waits for the epilogue's drain itself
   } else if (warp == kUWarp) {
     // ---------------------------------------------------------- U producer (all positions, lane 0)
     if (lane == 0) {
@@ -957,6 +1047,73 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
     const uint32_t idesc_pair = idesc_bf16_f32(kMTile, 2 * kTileN, false, true);
     const uint32_t idesc_one = idesc_bf16_f32(kMTile, kTileN, false, true);
     int issued = 0;  // any MMA issued
+    if constexpr (kLm) {
+      // pair gp's LM part: its accumulators start from h . W_lm (A = h rows in
+      // a U stage, K-major SW128: K-steps 32 bytes apart in each 64-element box)
+      auto lm_part = [&](int gp) -> bool {
+        const int j = gp % npair, pa = gp % kDraftAccPairs;
+        if (!mbar_wait(bar_tempty + 8 * pa, ((gp / kDraftAccPairs) & 1) ^ 1, abort_flag)) return false;
+        tc_fence_after_sync();
+        const uint32_t idesc = 2 * j + 1 < ntile ? idesc_pair : idesc_one;
+        const uint32_t d = tmem_base + static_cast<uint32_t>(pa * 2 * kTileN);
+        for (int kc = 0; kc < nkl; ++kc) {
+          const int gh = gp * nkl + kc, hs = gh % kDraftUStages;
+          const int g = gp * nkw + kc, sw = g % kDraftWStages;
+          if (!mbar_wait(bar_ufull + 8 * hs, (gh / kDraftUStages) & 1, abort_flag) ||
+              !mbar_wait(bar_wfull + 8 * sw, static_cast<uint32_t>(g / kDraftWStages) & 1u, abort_flag))
+            return false;
+          tc_fence_after_sync();
+          const uint64_t bdesc = smem_desc_sw128(base + plan.w(sw), kDraftWBox, 1024);
+          const uint32_t a0 = base + plan.u(hs);
+#pragma unroll
+          for (int q4 = 0; q4 < kDraftKChunk / 16; ++q4)
+            umma_bf16(d, smem_desc_sw128(a0 + (q4 >> 2) * (kDraftUBytes / 2) + (q4 & 3) * 32, 16, 1024),
+                      bdesc + static_cast<uint64_t>(q4 * 128), idesc, (kc | q4) != 0 ? 1u : 0u);
+          umma_commit(bar_wempty + 8 * sw);
+          umma_commit(bar_uempty + 8 * hs);
+          issued = 1;
+        }
+        return true;
+      };
+      // pair gp's bias part (A = W1 rows in tensor memory), then the pair is done
+      auto bias_part = [&](int gp) -> bool {
+        const int j = gp % npair, pa = gp % kDraftAccPairs;
+        const uint32_t idesc = 2 * j + 1 < ntile ? idesc_pair : idesc_one;
+        const uint32_t d = tmem_base + static_cast<uint32_t>(pa * 2 * kTileN);
+        for (int kw = 0; kw < nkc; ++kw) {
+          const int g = gp * nkw + nkl + kw, sw = g % kDraftWStages;
+          if (!mbar_wait(bar_wfull + 8 * sw, static_cast<uint32_t>(g / kDraftWStages) & 1u, abort_flag)) return false;
+          tc_fence_after_sync();
+          const int ks0 = kw * (kc_rows / 16), nks = min(kc_rows, p.rank - kw * kc_rows) / 16;
+          const uint64_t desc0 = smem_desc_sw128(base + plan.w(sw), w_box, 1024);
+#pragma unroll
+          for (int q4 = 0; q4 < kDraftKChunk / 16; ++q4)
+            if (q4 < nks) umma_bf16_ts(d, tmem_a + (ks0 + q4) * 8, desc0 + static_cast<uint64_t>(q4 * 128), idesc, 1u);
+          umma_commit(bar_wempty + 8 * sw);
+          issued = 1;
+        }
+        umma_commit(bar_tfull + 8 * pa);
+        return true;
+      };
+      for (int step = 0; step < p.gamma; ++step) {
+        // the first pair's LM part needs no A operand: it runs while the
+        // previous position's samplers are at work
+        if (lane == 0 && !*abort_flag && !lm_part(step * npair)) *abort_flag = 1;
+        __syncwarp();
+        named_barrier(2, kEpiThreads + 32);  // this position's A operand is in tensor memory
+        tc_fence_after_sync();
+        if (lane == 0 && !*abort_flag) {
+          for (int j = 0; j < npair; ++j) {
+            const int gp = step * npair + j;
+            if ((j > 0 && !lm_part(gp)) || !bias_part(gp)) {
+              *abort_flag = 1;
+              break;
+            }
+          }
+        }
+        __syncwarp();
+      }
+    } else
     for (int step = 0; step < p.gamma; ++step) {
       named_barrier(2, kEpiThreads + 32);  // this position's A operand is in tensor memory
       tc_fence_after_sync();
@@ -1196,7 +1353,7 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
       } else {
         // all 8 epilogue warps on each of this CTA's requests in turn
         for (int rr = blockIdx.x; rr < p.R; rr += gridDim.x) {
-          const int rc = sample_cta(p, &tm_slab, rr, step, warp - 2, ssm, slab_phase, abort_flag);
+          const int rc = sample_cta<kLm>(p, &tm_slab, &tm_lmslab, rr, step, warp - 2, ssm, slab_phase, abort_flag);
           if (rc < 0) {
             *abort_flag = 1;
             break;
@@ -1338,13 +1495,50 @@ int vocab_chunks(int n_tiles, int n_mtiles) {
   return c;
 }
 
-int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors, int R,
-                        int gamma, int V, int rank, float temperature, uint64_t seed, uint32_t round,
-                        int32_t* tokens, float* pd_tok, float* logZ, void* workspace, cudaStream_t stream) {
+// h [R, gamma, d] bf16 as a 3-D tensor (d, position, request), box
+// {64, 1, 128} with 128-byte swizzle: 64 hidden elements of one position for
+// the 128 rows of an M-tile, the K-major SW128 layout of the UMMA A operand.
+static int encode_h_map(CUtensorMap* tm, const uint16_t* h, int R, int gamma, int d) {
+  auto fn = get_encode_fn();
+  if (!fn) return DSPARK_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(gamma), static_cast<cuuint64_t>(R)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(gamma) * d * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kMTile)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult rc = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(h), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+// W_lm [d, V] bf16, box 32 columns x 256 rows without swizzle: one chunk of
+// the 32 columns the sampler recomputes ([256][32], 64-byte rows; rows past d
+// zero-filled).
+static int encode_lm_slab_map(CUtensorMap* tm, const uint16_t* W_lm, int V, int d) {
+  auto fn = get_encode_fn();
+  if (!fn) return DSPARK_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(d)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kSubN), 256};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult rc = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W_lm), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+// The draft with U given (U != null) or formed by the fused LM head from h
+// and W_lm (U == null, d > 0).
+static int launch_draft(const float* U, const uint16_t* h, const uint16_t* W_lm, int d, const uint16_t* W1,
+                        const uint16_t* W2, const int32_t* anchors, int R, int gamma, int V, int rank,
+                        float temperature, uint64_t seed, uint32_t round, int32_t* tokens, float* pd_tok, float* logZ,
+                        void* workspace, cudaStream_t stream) {
+  const bool lm = U == nullptr;
   const WorkspaceLayout L = workspace_layout(R, gamma, V);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DraftArgs a = {};
   a.U = U; a.W1 = W1; a.W2 = W2; a.anchors = anchors;
+  a.h = h; a.d = lm ? d : 0;
   a.tokens = tokens; a.pd_tok = pd_tok; a.logZ = logZ;
   a.centry = reinterpret_cast<unsigned long long*>(ws + L.coarse);
   a.fine = reinterpret_cast<unsigned long long*>(ws + L.fine);
@@ -1369,16 +1563,24 @@ int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
   if (a.n_chunks > kMaxSampleChunks || 2 * ceil_div(a.n_tiles, a.n_chunks) > kMaxSampleChunks || V > kMaxDraftV)
     return DSPARK_ERR_UNSUPPORTED_SHAPE;
 
-  CUtensorMap tm_w2, tm_u5, tm_u3, tm_slab;
-  std::memset(&tm_u5, 0, sizeof(tm_u5));  // not used unless R % 8 == 0
-  if (encode_w2_kchunk_map(&tm_w2, W2, V, rank) != DSPARK_OK || encode_u_half_map(&tm_u3, U, R, gamma, V) != DSPARK_OK ||
-      ((R & 7) == 0 && encode_u_fast_map(&tm_u5, U, R, gamma, V) != DSPARK_OK) ||
-      encode_w2_slab_map(&tm_slab, W2, V, rank) != DSPARK_OK)
+  CUtensorMap tm_w2, tm_u5, tm_u3, tm_slab, tm_lmslab;
+  std::memset(&tm_u5, 0, sizeof(tm_u5));  // not used unless R % 8 == 0 or with the LM head
+  std::memset(&tm_lmslab, 0, sizeof(tm_lmslab));  // used with the LM head only
+  if (encode_w2_kchunk_map(&tm_w2, W2, V, rank) != DSPARK_OK || encode_w2_slab_map(&tm_slab, W2, V, rank) != DSPARK_OK)
     return DSPARK_ERR_CUDA;
+  if (lm) {
+    if (encode_w2_kchunk_map(&tm_u5, W_lm, V, d) != DSPARK_OK || encode_h_map(&tm_u3, h, R, gamma, d) != DSPARK_OK ||
+        encode_lm_slab_map(&tm_lmslab, W_lm, V, d) != DSPARK_OK)
+      return DSPARK_ERR_CUDA;
+  } else if (encode_u_half_map(&tm_u3, U, R, gamma, V) != DSPARK_OK ||
+             ((R & 7) == 0 && encode_u_fast_map(&tm_u5, U, R, gamma, V) != DSPARK_OK)) {
+    return DSPARK_ERR_CUDA;
+  }
 
   const DraftSmem plan = draft_smem_plan(rank);
   const int max_smem = static_cast<int>(draft_smem_plan(256).total);
-  auto kernel = greedy ? k_markov_draft<true> : k_markov_draft<false>;
+  auto kernel = lm ? (greedy ? k_markov_draft<true, true> : k_markov_draft<false, true>)
+                  : (greedy ? k_markov_draft<true, false> : k_markov_draft<false, false>);
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   // the chunk entries and the sub-tile partials (no tag matches), the ready
@@ -1404,7 +1606,23 @@ int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tm_w2, tm_u5, tm_u3, tm_slab, a) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kernel, tm_w2, tm_u5, tm_u3, tm_slab, tm_lmslab, a) == cudaSuccess ? DSPARK_OK
+                                                                                         : DSPARK_ERR_CUDA;
+}
+
+int launch_markov_draft(const float* U, const uint16_t* W1, const uint16_t* W2, const int32_t* anchors, int R,
+                        int gamma, int V, int rank, float temperature, uint64_t seed, uint32_t round,
+                        int32_t* tokens, float* pd_tok, float* logZ, void* workspace, cudaStream_t stream) {
+  return launch_draft(U, nullptr, nullptr, 0, W1, W2, anchors, R, gamma, V, rank, temperature, seed, round, tokens,
+                      pd_tok, logZ, workspace, stream);
+}
+
+int launch_markov_draft_lmhead(const uint16_t* h, const uint16_t* W_lm, int d, const uint16_t* W1, const uint16_t* W2,
+                               const int32_t* anchors, int R, int gamma, int V, int rank, float temperature,
+                               uint64_t seed, uint32_t round, int32_t* tokens, float* pd_tok, float* logZ,
+                               void* workspace, cudaStream_t stream) {
+  return launch_draft(nullptr, h, W_lm, d, W1, W2, anchors, R, gamma, V, rank, temperature, seed, round, tokens,
+                      pd_tok, logZ, workspace, stream);
 }
 
 }  // namespace dspark

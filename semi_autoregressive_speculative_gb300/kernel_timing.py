@@ -2,6 +2,7 @@
 
     python -m semi_autoregressive_speculative_gb300.kernel_timing confidence [--calls 40]
     python -m semi_autoregressive_speculative_gb300.kernel_timing verify [--calls 20]
+    python -m semi_autoregressive_speculative_gb300.kernel_timing lmhead [--calls 5]
 
 ``confidence``: dspark_confidence at the batch-128 shape (R=128, gamma=16,
 d=4096) and at R=256, gamma=16, d=7168, called back to back on rotating h
@@ -9,7 +10,10 @@ buffers whose total exceeds the L2, so that h streams from HBM as it does in a
 round; CUDA events around the whole run.  ``verify``: dspark_verify, plain and
 with the optional c* output, on the batch-128 workload's own state (draft,
 synthetic target logits, confidence and early-stop schedule), CUDA events
-around each call.  Prints one JSON line per measurement.
+around each call.  ``lmhead``: dspark_markov_draft_lmhead at the batch-128
+shape (R=128, gamma=16, V=151936, d=4096) at T=1 and T=0, CUDA events around
+each call, with its dominant traffic: W_lm read once per position,
+gamma * d * V * 2 bytes a call.  Prints one JSON line per measurement.
 """
 from __future__ import annotations
 
@@ -99,13 +103,49 @@ def time_verify(calls: int) -> None:
                           "ms": float(np.median(ts)), "status": dr.status()}), flush=True)
 
 
+def time_lmhead(calls: int) -> None:
+    import torch
+    from . import dspark_markov_draft_lmhead, lib
+    wl = synth.WORKLOADS["r128_g16_v151936"]
+    dev = torch.device("cuda", 0)
+    W1, W2, _ = synth.weights(wl)
+    W_lm = synth.lm_head_weight(wl)
+    h = np.stack([synth.hidden(wl, 0, r) for r in range(wl.R)])
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    hd, Wl, W1d, W2d = t(h.view(np.int16)), t(W_lm.view(np.int16)), t(W1.view(np.int16)), t(W2.view(np.int16))
+    ad = t(synth.anchors(wl, 0).astype(np.int32))
+    tok = torch.empty((wl.R, wl.gamma), dtype=torch.int32, device=dev)
+    pd = torch.empty((wl.R, wl.gamma), dtype=torch.float32, device=dev)
+    lz = torch.empty_like(pd)
+    ws = torch.zeros(lib().dspark_workspace_size(wl.R, wl.gamma, wl.V, wl.rank, wl.d), dtype=torch.uint8, device=dev)
+    wlm_bytes = wl.gamma * wl.d * wl.V * 2
+    for temperature in (1.0, 0.0):
+        for _ in range(2):
+            dspark_markov_draft_lmhead(hd, Wl, W1d, W2d, ad, temperature, wl.seed, 0, tok, pd, lz, ws)
+        ts = []
+        for _ in range(calls):
+            e0, e1 = _events()
+            e0.record()
+            dspark_markov_draft_lmhead(hd, Wl, W1d, W2d, ad, temperature, wl.seed, 0, tok, pd, lz, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = float(np.median(ts))
+        print(json.dumps({"call": "dspark_markov_draft_lmhead", "temperature": temperature, "R": wl.R,
+                          "gamma": wl.gamma, "V": wl.V, "d": wl.d, "ms": ms, "W_lm_bytes": wlm_bytes,
+                          "W_lm_GBps": wlm_bytes / (ms * 1e-3) / 1e9,
+                          "status": int(ws[:4].view(torch.int32).item())}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("what", choices=["confidence", "verify"])
+    ap.add_argument("what", choices=["confidence", "verify", "lmhead"])
     ap.add_argument("--calls", type=int, default=40)
     args = ap.parse_args(argv)
     if args.what == "confidence":
         time_confidence(args.calls)
+    elif args.what == "lmhead":
+        time_lmhead(args.calls)
     else:
         time_verify(args.calls)
 

@@ -25,6 +25,7 @@ import numpy as np
 _S_W1, _S_W2, _S_W = 11, 12, 13
 _S_ANCHOR = 21
 _S_U, _S_H, _S_TNOISE, _S_BONUS, _S_FAKE = 31, 32, 33, 34, 35
+_S_WLM = 14
 
 
 @dataclass(frozen=True)
@@ -108,6 +109,20 @@ def weights(wl: Workload):
     W2 = to_bf16_bits(_rng(wl.seed, _S_W2).standard_normal((wl.rank, wl.V), np.float32) * wl.w_std)
     w = (_rng(wl.seed, _S_W).standard_normal(wl.d + wl.rank, np.float32) * wl.conf_w_std)
     return W1, W2, w.astype(np.float32)
+
+
+def lm_head_weight(wl: Workload, rows_per_block: int = 256) -> np.ndarray:
+    """W_lm bf16 bits [d, V] for the fused LM-head draft: normal entries scaled
+    so that h . W_lm has the spread of the workload's base logits
+    (u_std / (h_std * sqrt(d))).  Drawn in blocks of rows to bound the host
+    memory at full size."""
+    scale = np.float32(wl.u_std / (wl.h_std * np.sqrt(wl.d)))
+    out = np.empty((wl.d, wl.V), np.uint16)
+    for i0 in range(0, wl.d, rows_per_block):
+        i1 = min(wl.d, i0 + rows_per_block)
+        g = _rng(wl.seed, _S_WLM, i0)
+        out[i0:i1] = to_bf16_bits(g.standard_normal((i1 - i0, wl.V), np.float32) * scale)
+    return out
 
 
 def anchors(wl: Workload, rnd: int = 0) -> np.ndarray:

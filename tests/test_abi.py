@@ -65,6 +65,27 @@ def test_draft_validation(L):
     assert _draft(L, R=0) == 0               # empty batch: nothing to do
 
 
+def _draft_lm(L, R=4, gamma=7, V=4096, rank=256, d=256, T=1.0, h=FAKE, W_lm=FAKE, ws=FAKE, wsb=1 << 30):
+    return L.dspark_markov_draft_lmhead(h, W_lm, FAKE, FAKE, FAKE, R, gamma, V, rank, d, T, 0, 0, FAKE, FAKE, FAKE,
+                                        ws, wsb, None)
+
+
+def test_lmhead_draft_validation(L):
+    assert _draft_lm(L, d=0) == -1
+    assert _draft_lm(L, d=200) == -2         # d % 128
+    assert _draft_lm(L, d=65536 + 128) == -2
+    assert _draft_lm(L, V=4100) == -2
+    assert _draft_lm(L, rank=100) == -2
+    assert _draft_lm(L, T=-1.0) == -1
+    assert _draft_lm(L, h=0) == -1
+    assert _draft_lm(L, W_lm=0) == -1
+    assert _draft_lm(L, h=FAKE + 4) == -1    # misaligned
+    assert _draft_lm(L, W_lm=FAKE + 8) == -1
+    assert _draft_lm(L, ws=FAKE + 16) == -1
+    assert _draft_lm(L, wsb=100) == -1
+    assert _draft_lm(L, R=0) == 0
+
+
 def test_schedule_validation(L):
     def call(R=4, gamma=7, sps_len=4 * 8 + 1, mode=0, a=FAKE):
         return L.dspark_schedule(a, R, gamma, FAKE, sps_len, mode, 0, FAKE, FAKE, FAKE, FAKE, FAKE, 4, None)
