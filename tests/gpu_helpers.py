@@ -166,6 +166,45 @@ def check_draft(wl, inp, tok_g, pd_g, lz_g, temperature, rnd, requests, counts=N
     return diverged, near_ties
 
 
+def check_draft_forced(wl, U_rows, anchors, tok_g, pd_g, lz_g, temperature, rnd, requests, cdf_tol=CDF_TOL,
+                       logz_tol=LOGZ_TOL, tie_tol=1e-4):
+    """Every position of every request in `requests` against the oracle's
+    distribution conditioned on the kernel's own previous token (teacher
+    forcing), so that a legitimate divergence early in a row does not end
+    the comparison of that row.  U_rows[r] is request r's U [gamma, V].  Each
+    drawn token must be the oracle's inverse-CDF draw of the same Philox u, or
+    one whose CDF interval lies within cdf_tol of u; greedy: the oracle's
+    argmax, or within tie_tol of it.  p_d and log Z are compared at every
+    position.  Returns the number of draws that differ from the oracle's."""
+    W1, W2, _ = weights(wl)
+
+    def one(r):
+        differ = 0
+        prev = int(anchors[r])
+        for j in range(wl.gamma):
+            xg = int(tok_g[r, j])
+            if temperature == 0.0:
+                z = oracle.draft_logits_f32(U_rows[r][j], W1, W2, prev)
+                xo = int(np.argmax(z))
+                if xg != xo:
+                    assert z[xo] - z[xg] < tie_tol, f"greedy token at r={r} j={j}: {xg} vs {xo}"
+                    differ += 1
+                assert pd_g[r, j] == 1.0
+                assert abs(lz_g[r, j] - float(z[xg])) <= logz_tol * max(1.0, abs(float(z[xg]))), (r, j)
+            else:
+                p, logZ = oracle.draft_probs(U_rows[r][j], W1, W2, prev, temperature)
+                u = oracle.uniform(wl.seed, rnd, int(r), j, 0)
+                xo = oracle.inverse_cdf(p, u)
+                if xg != xo:
+                    assert _inverse_cdf_legit(p, xg, u, cdf_tol), f"sampled token at r={r} j={j}: {xg} vs {xo}, u={u}"
+                    differ += 1
+                assert abs(pd_g[r, j] - p[xg]) <= PROB_TOL, (r, j, pd_g[r, j], p[xg])
+                assert abs(lz_g[r, j] - logZ) <= logz_tol * max(1.0, abs(logZ)), (r, j, lz_g[r, j], logZ)
+            prev = xg
+        return differ
+    return sum(par_map(one, [int(r) for r in requests]))
+
+
 # ------------------------------------------------------------------ verify inputs
 def verify_inputs(wl, inp, rnd, compare, temperature, lens=None, drafted=None):
     """Draft outputs fed to verify: the oracle's draft for the `compare`

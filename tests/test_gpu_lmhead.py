@@ -8,14 +8,12 @@ about 3 to 10 carries an error of about sqrt(d + rank) * 2^-24 times the
 running sum, about 2e-5, so the comparison allows 5e-4 on log Z and on the
 greedy top-two gap and 1e-4 on the CDF; p_d keeps its 1e-4.
 """
-import types
-
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_helpers import PROB_TOL, check_draft, host, sample_requests
+from gpu_helpers import PROB_TOL, check_draft_forced, host, sample_requests
 from semi_autoregressive_speculative_gb300 import synth
 
 LM_CDF_TOL = 1e-4
@@ -58,29 +56,13 @@ def _gpu_draft(wl, W1, W2, W_lm, h, anchors, temperature, rnd):
 
 
 def _check(wl, h, W_lm, anchors, tok, pd, lz, temperature, rnd, requests):
-    """check_draft on the oracle's U = h . W_lm of the compared requests only."""
-    req = np.asarray(list(requests))
+    """Every position of the compared requests against the oracle drafting
+    from its U = h . W_lm, conditioned on the kernel's own previous tokens."""
+    req = [int(r) for r in requests]
     rows = oracle.lm_head_logits(h[req], W_lm)  # one pass over W_lm for all compared rows
-    inp = types.SimpleNamespace(U=_Rows({int(r): rows[i] for i, r in enumerate(req)}), anchors=anchors)
-    counts = {}
-    div, ties = check_draft(wl, inp, tok, pd, lz, temperature, rnd, req, counts=counts, cdf_tol=LM_CDF_TOL,
-                            logz_tol=LM_LOGZ_TOL, tie_tol=LM_TIE_TOL)
-    return div, ties, counts["compared"]
-
-
-class _Rows:
-    """U [R, gamma, V] of which only some requests' rows are formed: indexed
-    by a request, an array of requests or (request, position)."""
-
-    def __init__(self, rows):
-        self.rows = rows
-
-    def __getitem__(self, key):
-        if isinstance(key, tuple):
-            return self.rows[int(key[0])][key[1:]]
-        if isinstance(key, np.ndarray):
-            return np.stack([self.rows[int(k)] for k in key])
-        return self.rows[int(key)]
+    U_rows = {r: rows[i] for i, r in enumerate(req)}
+    return check_draft_forced(wl, U_rows, anchors, tok, pd, lz, temperature, rnd, req, cdf_tol=LM_CDF_TOL,
+                              logz_tol=LM_LOGZ_TOL, tie_tol=LM_TIE_TOL)
 
 
 @pytest.mark.gpu
@@ -94,9 +76,8 @@ def test_lmhead_draft_matches_oracle_every_row(R, gamma, V, rank, d, temps):
         tok, pd, lz, status = _gpu_draft(wl, W1, W2, W_lm, h, anchors, temperature, rnd)
         assert status == 0
         assert np.all((tok >= 0) & (tok < V))
-        div, ties, compared = _check(wl, h, W_lm, anchors, tok, pd, lz, temperature, rnd, range(R))
-        assert compared >= 0.5 * R * gamma, (compared, R * gamma)
-        assert div + ties <= max(1, R // 4), (div, ties)
+        differ = _check(wl, h, W_lm, anchors, tok, pd, lz, temperature, rnd, range(R))
+        assert differ <= max(1, R * gamma // 10), differ
 
 
 @pytest.mark.gpu
@@ -112,8 +93,9 @@ def test_lmhead_draft_full_size_batch128(temperature):
     assert status == 0
     assert np.all((tok >= 0) & (tok < wl.V))
     req = sample_requests(wl.R)
-    div, ties, compared = _check(wl, h, W_lm, anchors, tok, pd, lz, temperature, rnd, req)
-    assert compared >= 0.5 * len(req) * wl.gamma, (compared, len(req) * wl.gamma)
-    assert div + ties <= max(1, len(req) // 4), (div, ties)
+    differ = _check(wl, h, W_lm, anchors, tok, pd, lz, temperature, rnd, req)
+    # every differing draw was checked to lie within the CDF tolerance; at this
+    # vocabulary about one draw in ten lands that close to a boundary
+    assert differ <= len(req) * wl.gamma // 4, differ
     if temperature > 0:
         assert np.all(pd > 0.0) and np.all(pd <= 1.0 + PROB_TOL)
