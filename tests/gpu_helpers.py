@@ -167,7 +167,7 @@ def check_draft(wl, inp, tok_g, pd_g, lz_g, temperature, rnd, requests, counts=N
 
 
 def check_draft_forced(wl, U_rows, anchors, tok_g, pd_g, lz_g, temperature, rnd, requests, cdf_tol=CDF_TOL,
-                       logz_tol=LOGZ_TOL, tie_tol=1e-4):
+                       logz_tol=LOGZ_TOL, tie_tol=1e-4, prob_tol=PROB_TOL):
     """Every position of every request in `requests` against the oracle's
     distribution conditioned on the kernel's own previous token (teacher
     forcing), so that a legitimate divergence early in a row does not end
@@ -198,7 +198,7 @@ def check_draft_forced(wl, U_rows, anchors, tok_g, pd_g, lz_g, temperature, rnd,
                 if xg != xo:
                     assert _inverse_cdf_legit(p, xg, u, cdf_tol), f"sampled token at r={r} j={j}: {xg} vs {xo}, u={u}"
                     differ += 1
-                assert abs(pd_g[r, j] - p[xg]) <= PROB_TOL, (r, j, pd_g[r, j], p[xg])
+                assert abs(pd_g[r, j] - p[xg]) <= prob_tol, (r, j, pd_g[r, j], p[xg])
                 assert abs(lz_g[r, j] - logZ) <= logz_tol * max(1.0, abs(logZ)), (r, j, lz_g[r, j], logZ)
             prev = xg
         return differ

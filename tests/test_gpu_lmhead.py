@@ -1,24 +1,32 @@
 """The fused LM-head draft (dspark_markov_draft_lmhead) against the oracle.
 
 The oracle forms U = h . W_lm (oracle.lm_head_logits: fp64 sums rounded once
-to fp32) and drafts from it exactly as for a given U; the kernel instead sums
-the d LM-head products and the rank bias products in one fp32 tensor-core
-accumulation.  One fp32 sum over d + rank = 4352 products of logits of size
-about 3 to 10 carries an error of about sqrt(d + rank) * 2^-24 times the
-running sum, about 2e-5, so the comparison allows 5e-4 on log Z and on the
-greedy top-two gap and 1e-4 on the CDF; p_d keeps its 1e-4.
+to fp32) and drafts from it exactly as for a given U.  The kernel instead sums
+the d LM-head products and the rank bias products of a logit in one fp32
+tensor-core accumulator, K = 16 products per MMA step, (d + rank) / 16 steps
+in all.  Allowing each step to lose one fp32 unit in the last place of a
+logit of magnitude up to 32 bounds the kernel's logit error by
+
+    E = (d + rank) / 16 * 2^-23 * 32        (1.0e-3 at d = 4096, 1.8e-3 at d = 7168)
+
+and the comparison allows E on log Z, 2E on a greedy top-two gap, on the CDF
+and on p_d (|dp| <= p (1 - p) * 2E), never less than the U-path draft's own
+tolerances.  Measured: about 7e-4 on the logits at d = 7168.
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_helpers import PROB_TOL, check_draft_forced, host, sample_requests
+from gpu_helpers import CDF_TOL, LOGZ_TOL, PROB_TOL, check_draft_forced, host, sample_requests
 from semi_autoregressive_speculative_gb300 import synth
 
-LM_CDF_TOL = 1e-4
-LM_LOGZ_TOL = 5e-4
-LM_TIE_TOL = 5e-4
+
+def lm_tolerances(wl):
+    E = (wl.d + wl.rank) / 16 * 2.0 ** -23 * 32.0
+    return dict(cdf_tol=max(CDF_TOL, 2 * E), logz_tol=max(LOGZ_TOL, E), tie_tol=max(1e-4, 2 * E),
+                prob_tol=max(PROB_TOL, 2 * E))
+
 
 BASE = synth.WORKLOADS["r128_g16_v151936"]
 SMALL = [
@@ -61,8 +69,7 @@ def _check(wl, h, W_lm, anchors, tok, pd, lz, temperature, rnd, requests):
     req = [int(r) for r in requests]
     rows = oracle.lm_head_logits(h[req], W_lm)  # one pass over W_lm for all compared rows
     U_rows = {r: rows[i] for i, r in enumerate(req)}
-    return check_draft_forced(wl, U_rows, anchors, tok, pd, lz, temperature, rnd, req, cdf_tol=LM_CDF_TOL,
-                              logz_tol=LM_LOGZ_TOL, tie_tol=LM_TIE_TOL)
+    return check_draft_forced(wl, U_rows, anchors, tok, pd, lz, temperature, rnd, req, **lm_tolerances(wl))
 
 
 @pytest.mark.gpu
@@ -80,13 +87,17 @@ def test_lmhead_draft_matches_oracle_every_row(R, gamma, V, rank, d, temps):
         assert differ <= max(1, R * gamma // 10), differ
 
 
+FULL = [("r128_g16_v151936", 1.0), ("r128_g16_v151936", 0.0), ("r256_g16_v129280_d7168", 1.0)]
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("temperature", [1.0, 0.0])
-def test_lmhead_draft_full_size_batch128(temperature):
-    """The batch-128 workload (R=128, gamma=16, V=151936, d=4096) with W_lm
-    [4096, 151936] on the device; sampled rows of every tensor-memory lane
-    quarter against the oracle."""
-    wl = BASE
+@pytest.mark.parametrize("name,temperature", FULL, ids=[f"{n}_T{t}" for n, t in FULL])
+def test_lmhead_draft_full_size(name, temperature):
+    """Full size with W_lm on the device: the batch-128 workload (R=128,
+    gamma=16, V=151936, d=4096; W_lm 1.25 GB) and the two-M-tile workload
+    (R=256, V=129280, d=7168; W_lm 1.85 GB); sampled rows of every
+    tensor-memory lane quarter of every M-tile against the oracle."""
+    wl = synth.WORKLOADS[name]
     rnd = 0
     W1, W2, W_lm, h, anchors = _inputs(wl, rnd)
     tok, pd, lz, status = _gpu_draft(wl, W1, W2, W_lm, h, anchors, temperature, rnd)
@@ -94,8 +105,8 @@ def test_lmhead_draft_full_size_batch128(temperature):
     assert np.all((tok >= 0) & (tok < wl.V))
     req = sample_requests(wl.R)
     differ = _check(wl, h, W_lm, anchors, tok, pd, lz, temperature, rnd, req)
-    # every differing draw was checked to lie within the CDF tolerance; at this
-    # vocabulary about one draw in ten lands that close to a boundary
+    # every differing draw was checked to lie within the CDF tolerance; at these
+    # vocabularies about one draw in ten lands that close to a boundary
     assert differ <= len(req) * wl.gamma // 4, differ
     if temperature > 0:
-        assert np.all(pd > 0.0) and np.all(pd <= 1.0 + PROB_TOL)
+        assert np.all(pd > 0.0) and np.all(pd <= 1.0 + lm_tolerances(wl)["prob_tol"])
