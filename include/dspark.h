@@ -96,10 +96,11 @@ int dspark_selftest_bounded_wait(void *workspace, void *stream);
  *   pd_tok   fp32 [R, gamma]      out: p_d(x_j)
  *   logZ     fp32 [R, gamma]      out: log Z_j (natural log, of z_j = logits / T)
  * Sizes: R >= 0, 1 <= gamma <= 64, 8 <= V <= 2^24 with V % 8 == 0, rank in {64,128,192,256}.
- * R == 0 enqueues nothing.  Enqueues one zeroing of the workspace's
- * synchronisation words and one cooperative kernel that keeps every CTA
- * resident for all gamma positions (one CTA per SM; it fails to launch, with
- * DSPARK_ERR_CUDA, when R needs more than one M-tile of 128 rows per SM).
+ * R == 0 enqueues nothing.  Enqueues a prologue kernel (zeroes the
+ * workspace's synchronisation words and partials, stages the anchors' W1 rows)
+ * and one cooperative kernel that keeps every CTA resident for all gamma
+ * positions (one CTA per SM; it fails to launch, with DSPARK_ERR_CUDA, when R
+ * needs more than one M-tile of 128 rows per SM).
  * The kernel's cross-CTA waits are bounded: a wait that gives up sets
  * DSPARK_STATUS_TIMEOUT and the outputs are then not valid.
  */

@@ -789,6 +789,38 @@ __device__ __forceinline__ void merge_partial(float mx, float sm, float& runM, f
   }
 }
 
+// The call's prologue, one launch before the draft kernel: zeroes the chunk
+// entries, the synchronisation words and (sampled draws) the 32-column
+// partials, so that no tag from an earlier call can match, and stages each
+// row's anchor W1 row in the gather order of the A-operand staging copy, so
+// that position 0 gathers its A operand from L2 in whole lines like every
+// later position (read straight from W1, the rows are cold HBM misses queued
+// behind the producers' first TMA streams).  An anchor outside [0, V) is
+// reported and replaced by token 0.
+__global__ void __launch_bounds__(256) k_draft_prologue(const DraftArgs p, uint4* coarse, size_t coarse_u4,
+                                                        uint4* dsync, size_t dsync_u4, uint4* fine, size_t fine_u4) {
+  const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t nth = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (size_t i = tid; i < coarse_u4; i += nth) coarse[i] = z;
+  for (size_t i = tid; i < dsync_u4; i += nth) dsync[i] = z;
+  for (size_t i = tid; i < fine_u4; i += nth) fine[i] = z;
+  const int half_u4 = p.rank / 16;  // uint4 (8 bf16) per half of a W1 row
+  const size_t staged = static_cast<size_t>(p.R) * 32;
+  for (size_t i = tid; i < staged; i += nth) {
+    const int r = static_cast<int>(i >> 5), u = static_cast<int>(i & 31);
+    if (u >= 2 * half_u4) continue;
+    int tok = p.anchors[r];
+    if (tok < 0 || tok >= p.V) {
+      if (u == 0) report(p.status, DSPARK_STATUS_BAD_TOKEN);
+      tok = 0;
+    }
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(tok) * p.rank) + u);
+    const int rr = r % kMTile, h = u / half_u4, k = u - h * half_u4;
+    p.abuf[((((static_cast<size_t>(r / kMTile) * 4 + (rr >> 5)) * 2 + h) * 16 + k) << 5) + (rr & 31)] = v;
+  }
+}
+
 // kLm: the fused LM head.  U is not read: each pair's accumulators start from
 // h_j . W_lm, computed by the same MMAs over d more rank rows (A = h rows of
 // the M-tile by TMA through the U stages, B = W_lm K-chunks through the W2
@@ -1194,25 +1226,10 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
       }
       if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
         uint32_t a[64];  // all loads first, then the tensor-memory stores
-        if (step == 0) {
-          int tok = -1;
-          if (valid) {
-            tok = p.anchors[r];
-            if (tok < 0 || tok >= p.V) {
-              report(p.status, DSPARK_STATUS_BAD_TOKEN);
-              tok = 0;
-            }
-          }
-          const uint4* src =
-              reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(tok < 0 ? 0 : tok) * p.rank) + h * half_u4;
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            uint4 wv = make_uint4(0, 0, 0, 0);
-            if (tok >= 0 && k < half_u4) wv = __ldg(src + k);
-            a[4 * k] = wv.x; a[4 * k + 1] = wv.y; a[4 * k + 2] = wv.z; a[4 * k + 3] = wv.w;
-          }
-        } else {
-          // the staged W1 rows of this M-tile's previous tokens (written by other CTAs: through L2)
+        {
+          // the staged W1 rows of this M-tile's previous tokens (the anchors at
+          // position 0, staged by the prologue; later, written by other CTAs:
+          // through L2)
           const uint4* src = p.abuf + ((((static_cast<size_t>(mtile) * 4 + q) * 2 + h) * 16) << 5) + lane;
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
@@ -1585,10 +1602,14 @@ static int launch_draft(const float* U, const uint16_t* h, const uint16_t* W_lm,
     return DSPARK_ERR_CUDA;
   // the chunk entries and the sub-tile partials (no tag matches), the ready
   // counters and the abort word start at zero on every call
-  if (cudaMemsetAsync(ws + L.coarse, 0, static_cast<size_t>(a.R_pad) * a.n_chunks * 8, stream) != cudaSuccess ||
-      cudaMemsetAsync(ws + L.dsync, 0, L.dsync_bytes, stream) != cudaSuccess ||
-      (!greedy && cudaMemsetAsync(ws + L.fine, 0, static_cast<size_t>(2 * a.n_tiles) * a.R_pad * 8, stream) != cudaSuccess))
-    return DSPARK_ERR_CUDA;
+  {
+    const size_t coarse_b = static_cast<size_t>(a.R_pad) * a.n_chunks * 8;
+    const size_t fine_b = greedy ? 0 : static_cast<size_t>(2 * a.n_tiles) * a.R_pad * 8;
+    k_draft_prologue<<<sm_count(), 256, 0, stream>>>(a, reinterpret_cast<uint4*>(ws + L.coarse), coarse_b / 16,
+                                                      reinterpret_cast<uint4*>(ws + L.dsync), (L.dsync_bytes + 15) / 16,
+                                                      reinterpret_cast<uint4*>(ws + L.fine), fine_b / 16);
+    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  }
 
 #ifdef DSPARK_DRAFT_TRACE
   if (g_trace && g_trace_bytes >= static_cast<size_t>(gamma) * a.n_chunks * a.n_mtiles * kTraceEvents * 8) {

@@ -85,6 +85,8 @@ def phases(tr: np.ndarray, R: int) -> dict:
     start, end = e["start"][0], e["end"][0]
     out["kernel_span"] = float(end.max() - start.min()) / 1e3
     out["setup_to_first_a"] = us(e["a_ready"][0] - start.min())
+    out["start_spread"] = float(start.max() - start.min()) / 1e3  # CTAs' set-up done, last minus first
+    out["setup_to_first_a_same_cta"] = us(e["a_ready"][0] - start)
     out["first_position_period"] = us(e["a_ready"][1] - e["a_ready"][0])
     out["last_position_a_to_end"] = float(end.max() - np.median(e["a_ready"][g - 1])) / 1e3
     return out
