@@ -111,7 +111,10 @@ enum TraceEvent {
   kEvCopyThird = 13,  // copier: the position's third pair of U is in tensor memory (issued)
   kEvStart = 14,      // the CTA's set-up is done (position 0's slot only)
   kEvEnd = 15,        // the CTA is about to free its tensor memory and exit (position 0's slot only)
-  kTraceEvents = 16
+  kEvLaunch = 16,     // the CTA's first instruction (position 0's slot only)
+  kEvProStart = 17,   // prologue block b (b < the draft's CTA count) starts (position 0, CTA b)
+  kEvProEnd = 18,     // prologue block b is done (position 0, CTA b)
+  kTraceEvents = 19
 };
 #ifdef DSPARK_DRAFT_TRACE
 #define DRAFT_TRACE(p, step, ev)                                                                         \
@@ -799,6 +802,10 @@ __device__ __forceinline__ void merge_partial(float mx, float sm, float& runM, f
 // reported and replaced by token 0.
 __global__ void __launch_bounds__(256) k_draft_prologue(const DraftArgs p, uint4* coarse, size_t coarse_u4,
                                                         uint4* dsync, size_t dsync_u4, uint4* fine, size_t fine_u4) {
+#ifdef DSPARK_DRAFT_TRACE
+  const bool stamp = p.trace && threadIdx.x == 0 && static_cast<int>(blockIdx.x) < p.n_chunks * p.n_mtiles;
+  if (stamp) p.trace[static_cast<size_t>(blockIdx.x) * kTraceEvents + kEvProStart] = global_ns();
+#endif
   const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t nth = static_cast<size_t>(gridDim.x) * blockDim.x;
   const uint4 z = make_uint4(0, 0, 0, 0);
@@ -819,6 +826,10 @@ __global__ void __launch_bounds__(256) k_draft_prologue(const DraftArgs p, uint4
     const int rr = r % kMTile, h = u / half_u4, k = u - h * half_u4;
     p.abuf[((((static_cast<size_t>(r / kMTile) * 4 + (rr >> 5)) * 2 + h) * 16 + k) << 5) + (rr & 31)] = v;
   }
+#ifdef DSPARK_DRAFT_TRACE
+  __syncthreads();
+  if (stamp) p.trace[static_cast<size_t>(blockIdx.x) * kTraceEvents + kEvProEnd] = global_ns();
+#endif
 }
 
 // kLm: the fused LM head.  U is not read: each pair's accumulators start from
@@ -831,6 +842,7 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
     k_markov_draft(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u5,
                    const __grid_constant__ CUtensorMap tm_u3, const __grid_constant__ CUtensorMap tm_slab,
                    const __grid_constant__ CUtensorMap tm_lmslab, const DraftArgs p) {
+  if (threadIdx.x == 0) DRAFT_TRACE(p, 0, kEvLaunch);
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1602,6 +1614,12 @@ static int launch_draft(const float* U, const uint16_t* h, const uint16_t* W_lm,
     return DSPARK_ERR_CUDA;
   // the chunk entries and the sub-tile partials (no tag matches), the ready
   // counters and the abort word start at zero on every call
+#ifdef DSPARK_DRAFT_TRACE
+  if (g_trace && g_trace_bytes >= static_cast<size_t>(gamma) * a.n_chunks * a.n_mtiles * kTraceEvents * 8) {
+    a.trace = g_trace;
+    if (cudaMemsetAsync(g_trace, 0, g_trace_bytes, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  }
+#endif
   {
     const size_t coarse_b = static_cast<size_t>(a.R_pad) * a.n_chunks * 8;
     const size_t fine_b = greedy ? 0 : static_cast<size_t>(2 * a.n_tiles) * a.R_pad * 8;
@@ -1611,12 +1629,6 @@ static int launch_draft(const float* U, const uint16_t* h, const uint16_t* W_lm,
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   }
 
-#ifdef DSPARK_DRAFT_TRACE
-  if (g_trace && g_trace_bytes >= static_cast<size_t>(gamma) * a.n_chunks * a.n_mtiles * kTraceEvents * 8) {
-    a.trace = g_trace;
-    if (cudaMemsetAsync(g_trace, 0, g_trace_bytes, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
-  }
-#endif
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks * a.n_mtiles);
   cfg.blockDim = dim3(kDraftKThreads);

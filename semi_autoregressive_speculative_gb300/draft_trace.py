@@ -23,7 +23,8 @@ from . import build as pkg_build
 from . import synth
 
 EVENTS = ["a_ready", "first_acc", "tiles_done", "entry", "poll_done", "chunk_found", "fine_loaded", "slab_issued",
-          "slab_landed", "picked", "published", "ready_seen", "copy_first", "copy_third", "start", "end"]
+          "slab_landed", "picked", "published", "ready_seen", "copy_first", "copy_third", "start", "end", "launch",
+          "pro_start", "pro_end"]
 K_MTILE, K_TILE_N, K_MAX_CHUNKS = 128, 64, 1024
 
 
@@ -87,6 +88,12 @@ def phases(tr: np.ndarray, R: int) -> dict:
     out["setup_to_first_a"] = us(e["a_ready"][0] - start.min())
     out["start_spread"] = float(start.max() - start.min()) / 1e3  # CTAs' set-up done, last minus first
     out["setup_to_first_a_same_cta"] = us(e["a_ready"][0] - start)
+    # before the kernel: the prologue launch, the gap to the draft's first instruction, the draft's set-up
+    launch, ps, pe = e["launch"][0], e["pro_start"][0], e["pro_end"][0]
+    out["prologue_span"] = float(pe.max() - ps.min()) / 1e3
+    out["prologue_end_to_first_launch"] = float(launch.min() - pe.max()) / 1e3
+    out["launch_spread"] = float(launch.max() - launch.min()) / 1e3
+    out["launch_to_setup_done"] = us(start - launch)
     out["first_position_period"] = us(e["a_ready"][1] - e["a_ready"][0])
     out["last_position_a_to_end"] = float(end.max() - np.median(e["a_ready"][g - 1])) / 1e3
     return out
