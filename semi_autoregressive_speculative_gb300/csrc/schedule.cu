@@ -1,9 +1,16 @@
 // Hardware-aware prefix scheduler ("DSpark" §4.1-4.3; "投机解码的新做法" page,
 // section "按负载决定验证多少").  One CTA of 1024 threads, everything in
 // shared memory, no host round trip:
-//   1. keys (a descending, j ascending, r ascending) packed into 64 bits,
-//      written in (j, r) order and sorted by a stable radix sort on their
-//      upper 32 bits (four 8-bit passes);
+//   1. keys (a descending, j ascending, r ascending) packed into 64 bits and
+//      sorted.  Survival products never rise along a request (each step
+//      multiplies by a confidence <= 1, and fp32 rounding is monotone), so
+//      each request's keys already form a sorted run and the order is a merge
+//      of R runs: ceil(log2 R) levels in which every key finds its place by a
+//      binary search of the partner run.  The keys are distinct, so this is
+//      exactly the sorted order.  Rows that do rise (a caller's own a, or
+//      values reported as non-finite) take the general path: a stable radix
+//      sort of the keys written in (j, r) order on their upper 32 bits (four
+//      8-bit passes);
 //   2. a -> Q.40 fixed point and an integer inclusive scan: S_b is the same for
 //      every summation order;
 //   3. Theta(b) = (R + S_b 2^-40) * SPS[R + b] in fp64 for every b;
@@ -107,6 +114,43 @@ __device__ void radix_sort_keys(uint64_t* b0, uint64_t* b1, int* hist) {
   // four passes: the last one wrote b0
 }
 
+// Number of keys in v[b0, b1) (sorted ascending) that are below x.
+__device__ __forceinline__ int count_below(const uint64_t* v, int b0, int b1, uint64_t x) {
+  while (b0 < b1) {
+    const int m = (b0 + b1) >> 1;
+    if (v[m] < x) b0 = m + 1;
+    else b1 = m;
+  }
+  return b0;
+}
+
+// Sorts a[0, n) (distinct keys) whose runs [k run, (k + 1) run) are each
+// ascending, by merging adjacent runs level by level; b is scratch of the same
+// size.  On return a holds the sorted keys.
+__device__ void merge_sorted_runs(uint64_t* a, uint64_t* b, int n, int run) {
+  uint64_t* src = a;
+  uint64_t* dst = b;
+  for (int L = run; L < n; L <<= 1) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint64_t x = src[i];
+      const int lo = (i / (2 * L)) * (2 * L);
+      const int mid = min(lo + L, n), hi = min(lo + 2 * L, n);
+      // its index in its own run plus the keys of the partner run below it
+      const int pos = i < mid ? i + (count_below(src, mid, hi, x) - mid)
+                              : lo + (i - mid) + (count_below(src, lo, mid, x) - lo);
+      dst[pos] = x;
+    }
+    __syncthreads();
+    uint64_t* const tmp = src;
+    src = dst;
+    dst = tmp;
+  }
+  if (src != a) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) a[i] = src[i];
+    __syncthreads();
+  }
+}
+
 struct SchedSmem {
   uint32_t keys, S, rid, cnt, hist, total;
 };
@@ -144,7 +188,7 @@ __global__ void __launch_bounds__(kSchedThreads)
   pdl_wait();
   const int n = R * gamma;
   const int tid = threadIdx.x;
-  // 1. keys
+  // 1. keys, in (r, j) order: each request's run
   for (int i = tid; i < npow2; i += kSchedThreads) {
     uint64_t key = ~0ull;
     if (i < n) {
@@ -157,24 +201,37 @@ __global__ void __launch_bounds__(kSchedThreads)
       const int r = i / gamma, j = i - r * gamma;
       key = (static_cast<uint64_t>(0xFFFFFFFFu - bits) << 32) | (static_cast<uint64_t>(j) << 16) |
             static_cast<uint64_t>(r);
-      // stored in (j, r) order: the low key bits ascending, so that a stable
-      // sort by the upper 32 bits is the full 64-bit order
-      keys[j * R + r] = key;
-    } else {
-      keys[i] = key;
     }
+    keys[i] = key;
   }
   for (int r = tid; r < R; r += kSchedThreads) cnt[r] = 0;
   __syncthreads();
-  // 2. stable radix sort by a, ascending key (npow2 = 1024 E, E <= 8: the host
-  // pads to 1024); the prefix-sum array is the scratch buffer
+  int rises = 0;  // some request's a rises along its positions
+  for (int i = tid; i < n; i += kSchedThreads)
+    if (i % gamma != 0 && keys[i] < keys[i - 1]) rises = 1;
+  rises = __syncthreads_or(rises);
+  // 2. sort, ascending key; the prefix-sum array is the scratch buffer
   {
     uint64_t* scratch = reinterpret_cast<uint64_t*>(S);
-    switch (npow2 / kSchedThreads) {
-      case 1: radix_sort_keys<1>(keys, scratch, hist); break;
-      case 2: radix_sort_keys<2>(keys, scratch, hist); break;
-      case 4: radix_sort_keys<4>(keys, scratch, hist); break;
-      default: radix_sort_keys<8>(keys, scratch, hist); break;
+    if (!rises) {
+      merge_sorted_runs(keys, scratch, n, gamma);
+    } else {
+      // the keys in (j, r) order, the low key bits ascending, so that a stable
+      // sort by the upper 32 bits is the full 64-bit order (npow2 = 1024 E,
+      // E <= 8: the host pads to 1024; the padding keys stay at the end)
+      for (int i = tid; i < n; i += kSchedThreads) scratch[i] = keys[i];
+      __syncthreads();
+      for (int i = tid; i < n; i += kSchedThreads) {
+        const int r = i / gamma, j = i - r * gamma;
+        keys[j * R + r] = scratch[i];
+      }
+      __syncthreads();
+      switch (npow2 / kSchedThreads) {
+        case 1: radix_sort_keys<1>(keys, scratch, hist); break;
+        case 2: radix_sort_keys<2>(keys, scratch, hist); break;
+        case 4: radix_sort_keys<4>(keys, scratch, hist); break;
+        default: radix_sort_keys<8>(keys, scratch, hist); break;
+      }
     }
   }
   // 3. fixed-point values and request ids in sorted order; S[0] = 0

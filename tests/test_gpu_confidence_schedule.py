@@ -114,6 +114,24 @@ def test_schedule_random(R, gamma, seed):
         _assert_same(got, exp)
 
 
+@pytest.mark.parametrize("R,gamma,seed", [(4, 7, 10), (33, 5, 11), (128, 16, 12), (512, 16, 13), (100, 17, 14)])
+def test_schedule_rows_that_rise(R, gamma, seed):
+    """a that is not a survival product (it rises along some requests, and
+    has ties across requests): the kernel's general sort path, against the
+    oracle."""
+    from semi_autoregressive_speculative_gb300.round import DeviceRound
+    rng = np.random.default_rng(seed)
+    a = rng.uniform(0.0, 1.0, (R, gamma)).astype(np.float32)
+    a[rng.uniform(size=a.shape) < 0.05] = 0.5   # ties inside and across requests
+    dr = DeviceRound(R, gamma, 64, 64, 8)
+    knee = R * (1 + gamma) * rng.uniform(0.2, 0.9)
+    B = np.arange(R * (1 + gamma) + 1, dtype=np.float64)
+    sps = 1.0 / np.maximum(1.0, B / knee)
+    for mode, K in [(0, 0), (1, R * gamma // 3), (2, 0)]:
+        got, exp = _schedule_both(dr, a, sps, mode, K)
+        _assert_same(got, exp)
+
+
 def test_schedule_handbook_planner_inputs():
     # the page's adaptive-planner confidences, batch 512 x 7, against the oracle
     torch_ = pytest.importorskip("torch")

@@ -145,6 +145,15 @@ def test_status_flags_bad_anchor():
     assert dr.status() & DSPARK_STATUS_BAD_TOKEN
     dr.clear_status()
     assert dr.status() == 0
+    # greedy: the bad row drafts exactly as with anchor 0, the others as given
+    dr.draft(0.0, 0, 0)
+    tok = host(dr.tokens)
+    W1, W2, _ = weights(wl)
+    anchors = np.array(inp.anchors, np.int32)
+    anchors[1] = 0
+    tok_o, _, _ = oracle.draft(inp.U, W1, W2, anchors, 0.0, 0, 0)
+    assert np.array_equal(tok, tok_o), (tok, tok_o)
+    assert dr.status() & DSPARK_STATUS_BAD_TOKEN
 
 
 def test_nonfinite_logits_reported():
