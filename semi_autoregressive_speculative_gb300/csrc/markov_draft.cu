@@ -1,6 +1,10 @@
 // Markov-head sequential draft ("DSpark" §2.2 eq. p_k, §2.3 eq. B = W1 W2,
 // and the position-by-position loop of §6.2) as ONE persistent cooperative
-// kernel per call: every CTA stays resident for all gamma positions.
+// kernel per call: every CTA stays resident for all gamma positions.  A small
+// prologue kernel before it clears the call's tagged words and stages the
+// anchors' W1 rows (k_draft_prologue).  A compile-time variant takes the
+// pre-LM-head hidden states instead of U and forms U = h . W_lm in the same
+// MMAs (kLm, "DSpark: Speculative decodingを活用した…", "隠れ状態通信").
 //
 // Per position j, on every CTA (one contiguous V-chunk of one 128-row M-tile):
 //   gather   each row's W1[x_{j-1}] goes into tensor memory as the UMMA A
