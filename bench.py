@@ -332,8 +332,8 @@ def run_gpu(args):
     cstar_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(cstar_graph, stream=stream):
         dr.verify(temp, seed, rnd, c_star=True)
-    # draft: one persistent kernel; confidence 1; schedule 1; verify 3 (greedy) or 5
-    launches_per_step = 1 + 1 + 1 + (3 if temp == 0 else 5)
+    # draft: a prologue kernel and one persistent kernel; confidence 1; schedule 1; verify 3 (greedy) or 5
+    launches_per_step = 2 + 1 + 1 + (3 if temp == 0 else 5)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
