@@ -928,6 +928,13 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
   // then the nkc of W2: nkw ring stages per pair in all
   const int nkl = kLm ? p.d / kDraftKChunk : 0;
   const int nkw = nkl + nkc;
+  // with the LM head, pairs go through the MMA two at a time (a group), so
+  // that each h K-chunk is loaded once for both: a group's ring stages are
+  // its W_lm chunks, the two pairs' interleaved chunk by chunk, then the W2
+  // chunks of its first pair, then of its second.  Group m of a position
+  // holds pairs 2m and 2m + 1; without the LM head a group is one pair.
+  constexpr int kGroup = kLm ? 2 : 1;
+  const int ngroup = (npair + kGroup - 1) / kGroup;
 
   if (warp == 0) {
     // ---------------------------------------------------------- W2 producer (all positions, lane 0)
@@ -937,13 +944,25 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
       uint32_t wlast = 0;  // per stage s: bit 2s = filled, bit 2s + 1 = parity of its last fill
       bool ok = true;
       for (int step = 0; step < p.gamma && ok; ++step) {
-        for (int j = 0; j < npair && ok; ++j) {
-          const int gp = step * npair + j;
-          const bool two = 2 * j + 1 < ntile;
-          const int va = (t_begin + tile_of(step, 2 * j, ntile)) * kTileN;
-          const int vb = two ? (t_begin + tile_of(step, 2 * j + 1, ntile)) * kTileN : 0;
-          for (int kc = 0; kc < nkw; ++kc) {
-            const int g = gp * nkw + kc;
+        for (int j0 = 0; j0 < npair && ok; j0 += kGroup) {
+          const int nb = min(kGroup, npair - j0);
+          for (int t = 0; t < nb * nkw; ++t) {
+            // the group's t-th ring stage: W_lm chunk kc of member b, or W2 chunk kw of member b
+            int b, kc, kw;
+            if (t < nkl * nb) {
+              b = t % nb;
+              kc = t / nb;
+              kw = -1;
+            } else {
+              b = (t - nkl * nb) / nkc;
+              kw = t - nkl * nb - b * nkc;
+              kc = -1;
+            }
+            const int j = j0 + b;
+            const bool two = 2 * j + 1 < ntile;
+            const int va = (t_begin + tile_of(step, 2 * j, ntile)) * kTileN;
+            const int vb = two ? (t_begin + tile_of(step, 2 * j + 1, ntile)) * kTileN : 0;
+            const int g = (step * npair + j0) * nkw + t;
             const int sw = g % kDraftWStages;
             const uint32_t par = static_cast<uint32_t>(g / kDraftWStages) & 1u;
             if (!mbar_wait(bar_wempty + 8 * sw, par ^ 1u, abort_flag)) {
@@ -951,7 +970,7 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
               ok = false;
               break;
             }
-            if (kLm && kc < nkl) {
+            if (kLm && kc >= 0) {
               // W_lm rows [kc * 128, kc * 128 + 128) of both tiles (streamed: evict first)
               mbar_arrive_expect_tx(bar_wfull + 8 * sw, (two ? 2u : 1u) * kDraftWBox);
               tma_load_2d(base + plan.w(sw), &tm_u5, bar_wfull + 8 * sw, va, kc * kDraftKChunk, pol_lm);
@@ -959,7 +978,6 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
             } else {
               // rank rows [kw * kc_rows, (kw + 1) * kc_rows) of both tiles; rows past the
               // rank and columns past V are zero-filled
-              const int kw = kc - nkl;
               mbar_arrive_expect_tx(bar_wfull + 8 * sw, (two ? 2u : 1u) * w_box);
               tma_load_2d(base + plan.w(sw), &tm_w2, bar_wfull + 8 * sw, va, kw * kc_rows, pol_w);
               if (two) tma_load_2d(base + plan.w(sw) + w_box, &tm_w2, bar_wfull + 8 * sw, vb, kw * kc_rows, pol_w);
@@ -980,16 +998,16 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
     __syncwarp();
   } else if (kLm && warp == kUWarp) {
     // ---------------------------------------------------------- h producer (LM head; all positions, lane 0)
-    // each LM K-chunk of a pair: the M-tile's h rows at this position, K
-    // elements [kc * 128, kc * 128 + 128) as two 64-element SW128 boxes (rows
-    // past R zero-filled), into a U stage
+    // each LM K-chunk of a group of pairs: the M-tile's h rows at this
+    // position, K elements [kc * 128, kc * 128 + 128) as two 64-element SW128
+    // boxes (rows past R zero-filled), into a U stage
     if (lane == 0) {
-      const uint64_t pol_h = policy_evict_last();  // reread by every pair of the position
+      const uint64_t pol_h = policy_evict_last();  // reread by every group of the position
       int hfilled = 0;
-      for (int gp = 0; gp < npair * p.gamma && !*abort_flag; ++gp) {
-        const int step = gp / npair;
+      for (int gg = 0; gg < ngroup * p.gamma && !*abort_flag; ++gg) {
+        const int step = gg / ngroup;
         for (int kc = 0; kc < nkl; ++kc) {
-          const int gh = gp * nkl + kc, hs = gh % kDraftUStages;
+          const int gh = gg * nkl + kc, hs = gh % kDraftUStages;
           if (!mbar_wait(bar_uempty + 8 * hs, ((gh / kDraftUStages) & 1) ^ 1, abort_flag)) {
             *abort_flag = 1;
             break;
@@ -1096,40 +1114,62 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
     const uint32_t idesc_one = idesc_bf16_f32(kMTile, kTileN, false, true);
     int issued = 0;  // any MMA issued
     if constexpr (kLm) {
-      // pair gp's LM part: its accumulators start from h . W_lm (A = h rows in
-      // a U stage, K-major SW128: K-steps 32 bytes apart in each 64-element box)
-      auto lm_part = [&](int gp) -> bool {
-        const int j = gp % npair, pa = gp % kDraftAccPairs;
-        if (!mbar_wait(bar_tempty + 8 * pa, ((gp / kDraftAccPairs) & 1) ^ 1, abort_flag)) return false;
+      // group m's LM part: the accumulators of its one or two pairs start from
+      // h . W_lm (A = h rows in a U stage, K-major SW128: K-steps 32 bytes
+      // apart in each 64-element box, shared by both pairs)
+      auto lm_group = [&](int step, int m) -> bool {
+        const int j0 = kGroup * m, nb = min(kGroup, npair - j0);
+        uint32_t dacc[kGroup], idsc[kGroup];
+#pragma unroll
+        for (int b = 0; b < kGroup; ++b) {
+          if (b >= nb) break;
+          const int gp = step * npair + j0 + b, pa = gp % kDraftAccPairs;
+          if (!mbar_wait(bar_tempty + 8 * pa, ((gp / kDraftAccPairs) & 1) ^ 1, abort_flag)) return false;
+          idsc[b] = 2 * (j0 + b) + 1 < ntile ? idesc_pair : idesc_one;
+          dacc[b] = tmem_base + static_cast<uint32_t>(pa * 2 * kTileN);
+        }
         tc_fence_after_sync();
-        const uint32_t idesc = 2 * j + 1 < ntile ? idesc_pair : idesc_one;
-        const uint32_t d = tmem_base + static_cast<uint32_t>(pa * 2 * kTileN);
         for (int kc = 0; kc < nkl; ++kc) {
-          const int gh = gp * nkl + kc, hs = gh % kDraftUStages;
-          const int g = gp * nkw + kc, sw = g % kDraftWStages;
-          if (!mbar_wait(bar_ufull + 8 * hs, (gh / kDraftUStages) & 1, abort_flag) ||
-              !mbar_wait(bar_wfull + 8 * sw, static_cast<uint32_t>(g / kDraftWStages) & 1u, abort_flag))
-            return false;
+          const int gh = (step * ngroup + m) * nkl + kc, hs = gh % kDraftUStages;
+          if (!mbar_wait(bar_ufull + 8 * hs, (gh / kDraftUStages) & 1, abort_flag)) return false;
+          int sw[kGroup];
+#pragma unroll
+          for (int b = 0; b < kGroup; ++b) {
+            if (b >= nb) break;
+            const int g = (step * npair + j0) * nkw + kc * nb + b;
+            sw[b] = g % kDraftWStages;
+            if (!mbar_wait(bar_wfull + 8 * sw[b], static_cast<uint32_t>(g / kDraftWStages) & 1u, abort_flag))
+              return false;
+          }
           tc_fence_after_sync();
-          const uint64_t bdesc = smem_desc_sw128(base + plan.w(sw), kDraftWBox, 1024);
           const uint32_t a0 = base + plan.u(hs);
 #pragma unroll
-          for (int q4 = 0; q4 < kDraftKChunk / 16; ++q4)
-            umma_bf16(d, smem_desc_sw128(a0 + (q4 >> 2) * (kDraftUBytes / 2) + (q4 & 3) * 32, 16, 1024),
-                      bdesc + static_cast<uint64_t>(q4 * 128), idesc, (kc | q4) != 0 ? 1u : 0u);
-          umma_commit(bar_wempty + 8 * sw);
+          for (int b = 0; b < kGroup; ++b) {
+            if (b >= nb) break;
+            const uint64_t bdesc = smem_desc_sw128(base + plan.w(sw[b]), kDraftWBox, 1024);
+#pragma unroll
+            for (int q4 = 0; q4 < kDraftKChunk / 16; ++q4)
+              umma_bf16(dacc[b], smem_desc_sw128(a0 + (q4 >> 2) * (kDraftUBytes / 2) + (q4 & 3) * 32, 16, 1024),
+                        bdesc + static_cast<uint64_t>(q4 * 128), idsc[b], (kc | q4) != 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int b = 0; b < kGroup; ++b) {
+            if (b >= nb) break;
+            umma_commit(bar_wempty + 8 * sw[b]);
+          }
           umma_commit(bar_uempty + 8 * hs);
           issued = 1;
         }
         return true;
       };
-      // pair gp's bias part (A = W1 rows in tensor memory), then the pair is done
-      auto bias_part = [&](int gp) -> bool {
-        const int j = gp % npair, pa = gp % kDraftAccPairs;
+      // member b of group m: its bias part (A = W1 rows in tensor memory), then the pair is done
+      auto bias_member = [&](int step, int m, int b) -> bool {
+        const int j0 = kGroup * m, nb = min(kGroup, npair - j0), j = j0 + b;
+        const int gp = step * npair + j, pa = gp % kDraftAccPairs;
         const uint32_t idesc = 2 * j + 1 < ntile ? idesc_pair : idesc_one;
         const uint32_t d = tmem_base + static_cast<uint32_t>(pa * 2 * kTileN);
         for (int kw = 0; kw < nkc; ++kw) {
-          const int g = gp * nkw + nkl + kw, sw = g % kDraftWStages;
+          const int g = (step * npair + j0) * nkw + nkl * nb + b * nkc + kw, sw = g % kDraftWStages;
           if (!mbar_wait(bar_wfull + 8 * sw, static_cast<uint32_t>(g / kDraftWStages) & 1u, abort_flag)) return false;
           tc_fence_after_sync();
           const int ks0 = kw * (kc_rows / 16), nks = min(kc_rows, p.rank - kw * kc_rows) / 16;
@@ -1144,16 +1184,18 @@ __global__ void __launch_bounds__(kDraftKThreads, 1)
         return true;
       };
       for (int step = 0; step < p.gamma; ++step) {
-        // the first pair's LM part needs no A operand: it runs while the
+        // the first group's LM part needs no A operand: it runs while the
         // previous position's samplers are at work
-        if (lane == 0 && !*abort_flag && !lm_part(step * npair)) *abort_flag = 1;
+        if (lane == 0 && !*abort_flag && !lm_group(step, 0)) *abort_flag = 1;
         __syncwarp();
         named_barrier(2, kEpiThreads + 32);  // this position's A operand is in tensor memory
         tc_fence_after_sync();
         if (lane == 0 && !*abort_flag) {
-          for (int j = 0; j < npair; ++j) {
-            const int gp = step * npair + j;
-            if ((j > 0 && !lm_part(gp)) || !bias_part(gp)) {
+          for (int m = 0; m < ngroup; ++m) {
+            bool ok = m == 0 || lm_group(step, m);
+            const int nb = min(kGroup, npair - kGroup * m);
+            for (int b = 0; b < nb && ok; ++b) ok = bias_member(step, m, b);
+            if (!ok) {
               *abort_flag = 1;
               break;
             }
