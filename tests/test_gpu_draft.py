@@ -20,6 +20,10 @@ SMALL_CASES = [
     (synth.scaled(TINY, R=3, gamma=6, V=4104, rank=192, d=40, name="v4104_rank192"), (0.7, 0.0)),
     # three M-tiles: samplers of one M-tile run on CTAs of the others
     (synth.scaled(TINY, R=300, gamma=3, V=2056, d=16, name="r300_three_mtiles"), (1.0, 0.0)),
+    # the most positions the boundary accepts (position tags 1..64)
+    (synth.scaled(TINY, R=2, gamma=64, V=2048, d=16, name="g64_max_positions"), (1.0, 0.0)),
+    # nine M-tiles, the last with 76 rows
+    (synth.scaled(TINY, R=1100, gamma=2, V=4104, d=16, name="r1100_nine_mtiles"), (1.0, 0.0)),
 ]
 
 
@@ -33,6 +37,23 @@ def test_draft_small(wl, temps):
         div, ties = check_draft(wl, inp, tok, pd, lz, temp, 0, range(wl.R))
         assert div <= max(1, wl.R * wl.gamma // 200)
         assert ties == 0
+    assert dr.status() == 0
+
+
+def test_draft_one_mtile_per_sm():
+    """The most rows one cooperative launch holds: one 128-row M-tile per SM,
+    each CTA alone on its M-tile's whole vocabulary."""
+    import torch
+    R = torch.cuda.get_device_properties(0).multi_processor_count * 128
+    wl = synth.scaled(TINY, R=R, gamma=1, V=512, d=16, name=f"r{R}_one_mtile_per_sm")
+    dr, inp = device_round(wl)
+    for temp in (1.0, 0.0):
+        dr.draft(temp, wl.seed, 0)
+        tok, pd, lz = host(dr.tokens), host(dr.pd), host(dr.logZ)
+        assert tok.min() >= 0 and tok.max() < wl.V
+        div, ties = check_draft(wl, inp, tok, pd, lz, temp, 0, range(wl.R))
+        assert div <= max(1, wl.R * wl.gamma // 200)
+        assert ties <= 2
     assert dr.status() == 0
 
 
