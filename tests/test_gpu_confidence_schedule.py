@@ -25,6 +25,7 @@ def _tokens(wl, seed=0):
     TINY,
     synth.scaled(TINY, R=7, gamma=5, V=1000, d=300, name="d300_odd"),     # d not a multiple of 8
     synth.scaled(TINY, R=3, gamma=33, V=64, d=8, rank=64, name="g33"),     # gamma > warps per CTA
+    synth.scaled(TINY, R=2, gamma=64, V=64, d=40, name="g64"),             # the most positions accepted
     synth.WORKLOADS["r128_g16_v151936"],
     synth.WORKLOADS["r256_g16_v129280_d7168"],
 ], ids=lambda w: w.name)

@@ -47,6 +47,15 @@ def test_verify_ragged_lengths(temperature):
     assert ex <= 1
 
 
+@pytest.mark.parametrize("temperature", [1.0, 0.0])
+def test_verify_max_positions(temperature):
+    # gamma = 64, the most positions the boundary accepts, lengths from 0 to 64
+    wl = synth.scaled(TINY, R=5, gamma=64, V=1000, d=16, name="verify_g64")
+    lens = np.array([0, 1, 31, 63, 64], np.int32)
+    na, nx, ex = _run(wl, temperature, range(wl.R), lens=lens)
+    assert ex <= 1
+
+
 def test_verify_many_rows_two_mtiles():
     wl = synth.scaled(TINY, R=140, gamma=3, V=2048, rank=128, d=16, name="verify_r140")
     na, nx, ex = _run(wl, 1.0, range(0, 140, 7))
