@@ -220,6 +220,33 @@ int dspark_verify(const float *T, const float *U, const uint16_t *W1, const uint
                   void *stream);
 
 /*
+ * dspark_load_verified_rows — bring into device memory, from page-locked host
+ * memory, exactly the target rows that dspark_verify reads: rows 0..lens[r]
+ * of each request r, the prefix the scheduler admitted for verification
+ * ("DSpark" §4.1-4.2: only the admitted positions are verified).  The pages
+ * have no counterpart: this entry point exists for callers whose target
+ * logits arrive in host memory.  lens is read on the device, so the ragged
+ * copy needs no device-to-host read of the lengths and no synchronisation;
+ * the SMs read the host memory over the host link (mapped memory), which
+ * leaves the copy engines free for other copies running at the same time.
+ *   T_host  fp32 [R, gamma+1, V]  HOST pointer: page-locked memory mapped into the
+ *                                 device's address space (cudaHostAlloc, cudaMallocHost
+ *                                 or cudaHostRegister on a device with unified
+ *                                 addressing); 16-byte aligned; owned by the caller
+ *   lens    int32 [R]             device; a length outside [0, gamma] is clamped and
+ *                                 sets DSPARK_STATUS_BAD_LENGTH
+ *   T       fp32 [R, gamma+1, V]  out, device: rows 0..lens[r] of request r are
+ *                                 written, all other rows are left as they were
+ *   workspace                     any 256-byte-aligned device buffer whose first int32
+ *                                 is the status word
+ * Sizes: R >= 0, 1 <= gamma <= 64, V >= 8 with V % 8 == 0.  R == 0 enqueues
+ * nothing.  Returns DSPARK_ERR_INVALID_ARG, enqueuing nothing, when T_host is
+ * not page-locked mapped host memory (pageable or device memory).  One kernel.
+ */
+int dspark_load_verified_rows(const float *T_host, const int32_t *lens, int R, int gamma, int V,
+                              float *T, void *workspace, void *stream);
+
+/*
  * dspark_markov_draft_noalloc — the Markov-head draft of dspark_markov_draft
  * without a caller workspace.  The pages have no counterpart: this entry point
  * exists for callers that cannot obtain device memory where they draft, such

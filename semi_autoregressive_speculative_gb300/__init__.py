@@ -27,7 +27,7 @@ MODE_EARLY_STOP, MODE_TOP_K, MODE_FIXED = 0, 1, 2
 
 EXPORTS = ("dspark_workspace_size", "dspark_clear_status", "dspark_markov_draft", "dspark_confidence",
            "dspark_schedule", "dspark_verify", "dspark_markov_draft_noalloc", "dspark_selftest_bounded_wait",
-           "dspark_markov_draft_lmhead")
+           "dspark_markov_draft_lmhead", "dspark_load_verified_rows")
 
 _lib = None
 
@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.dspark_schedule.argtypes = [P, I, I, P, I, I, I, P, P, P, P, P, SZ, P]
         L.dspark_verify.restype = I
         L.dspark_verify.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, U64, U32, P, P, P, P, SZ, P]
+        L.dspark_load_verified_rows.restype = I
+        L.dspark_load_verified_rows.argtypes = [P, P, I, I, I, P, P, P]
         L.dspark_markov_draft_noalloc.restype = I
         L.dspark_markov_draft_noalloc.argtypes = [P, P, P, P, I, I, I, I, F, U64, U32, P, P, P, P, P]
         _lib = L
@@ -167,6 +169,16 @@ def dspark_verify(T, U, W1, W2, anchors, tokens, pd_tok, logZ, lens, temperature
         _ptr(T), _ptr(U), _ptr(W1), _ptr(W2), _ptr(anchors), _ptr(tokens), _ptr(pd_tok), _ptr(logZ),
         _ptr(lens), R, gamma, V, rank, float(temperature), int(seed), int(round_), _ptr(n_accept),
         _ptr(next_token), _ptr(c_star), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def dspark_load_verified_rows(T_host, lens, T, workspace, stream=None) -> None:
+    """`T_host`: page-locked CPU fp32 tensor [R, gamma+1, V]; `lens`, `T` and
+    `workspace` on the device."""
+    R, g1, V = T.shape
+    if tuple(T_host.shape) != (R, g1, V):
+        raise ValueError(f"T_host must have shape {(R, g1, V)}, got {tuple(T_host.shape)}")
+    _check("dspark_load_verified_rows", lib().dspark_load_verified_rows(
+        _ptr(T_host), _ptr(lens), R, g1 - 1, V, _ptr(T), _ptr(workspace), _stream(stream)))
 
 
 def dspark_markov_draft_noalloc(U, W1, W2, anchors, temperature, seed, round_, tokens, pd_tok, logZ, status=None,

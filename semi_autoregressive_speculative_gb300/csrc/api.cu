@@ -24,6 +24,8 @@ int launch_verify(const float* T, const float* U, const uint16_t* W1, const uint
                   const int32_t* tokens, const float* pd_tok, const float* logZ, const int32_t* lens, int R, int gamma,
                   int V, int rank, float temperature, uint64_t seed, uint32_t round, int32_t* n_accept,
                   int32_t* next_token, float* c_star, void* workspace, cudaStream_t stream);
+int launch_load_verified_rows(const float* T_host, const int32_t* lens, int R, int gamma, int V, float* T,
+                              int32_t* status, cudaStream_t stream);
 
 int sm_count() {
   static int count[64] = {0};
@@ -132,6 +134,18 @@ int dspark_verify(const float* T, const float* U, const uint16_t* W1, const uint
   if (workspace_bytes < workspace_layout(R, gamma, V).total) return DSPARK_ERR_INVALID_ARG;
   return launch_verify(T, U, W1, W2, anchors, tokens, pd_tok, logZ, lens, R, gamma, V, rank, temperature, seed, round,
                        n_accept, next_token, c_star, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int dspark_load_verified_rows(const float* T_host, const int32_t* lens, int R, int gamma, int V, float* T,
+                              void* workspace, void* stream) {
+  if (R < 0 || gamma < 1 || V < 8) return DSPARK_ERR_INVALID_ARG;
+  if (gamma > kMaxGamma || V % 8 != 0) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (R == 0) return DSPARK_OK;
+  if (!T_host || !lens || !T || !workspace) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned16(T_host) || !aligned16(T) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return DSPARK_ERR_INVALID_ARG;
+  return launch_load_verified_rows(T_host, lens, R, gamma, V, T, static_cast<int32_t*>(workspace),
+                                   static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -3,7 +3,8 @@
 ``DeviceRound`` owns the device tensors of one workload shape (inputs,
 outputs, scratch workspace) and runs the round through the C ABI on the
 current torch stream: draft -> confidence -> schedule -> verify.  Target
-logits are an input of verify and are set by the caller.
+logits are an input of verify and are set by the caller, on the device or,
+for the admitted rows only, from page-locked host memory (load_target_rows).
 """
 from __future__ import annotations
 
@@ -11,7 +12,8 @@ import numpy as np
 import torch
 
 from . import (MODE_EARLY_STOP, MODE_FIXED, MODE_TOP_K, dspark_clear_status, dspark_confidence,
-               dspark_markov_draft, dspark_schedule, dspark_verify, dspark_workspace_size, read_status)
+               dspark_load_verified_rows, dspark_markov_draft, dspark_schedule, dspark_verify, dspark_workspace_size,
+               read_status)
 
 __all__ = ["DeviceRound", "MODE_EARLY_STOP", "MODE_TOP_K", "MODE_FIXED"]
 
@@ -78,6 +80,11 @@ class DeviceRound:
     def schedule(self, mode: int, budget_K: int = 0, a=None):
         dspark_schedule(self.a if a is None else a, self.sps, mode, budget_K, self.lens, self.sched_out[0:1],
                         self.sched_out[1:2], self.theta, self.workspace)
+
+    def load_target_rows(self, T_host):
+        """Copy rows 0..lens[r] of each request from the page-locked host
+        tensor T_host [R, gamma+1, V] into self.T (lens stays on the device)."""
+        dspark_load_verified_rows(T_host, self.lens, self.T, self.workspace)
 
     def verify(self, temperature: float, seed: int, rnd: int, tokens=None, pd=None, logZ=None, lens=None,
                c_star: bool = False):

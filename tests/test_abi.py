@@ -120,3 +120,21 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pkg, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         pkg.lib()
+
+
+def test_load_rows_validation(L):
+    def call(T_host=FAKE, lens=FAKE, R=4, gamma=7, V=4096, T=FAKE, ws=FAKE):
+        return L.dspark_load_verified_rows(T_host, lens, R, gamma, V, T, ws, None)
+    assert call(R=-1) == -1
+    assert call(gamma=0) == -1
+    assert call(V=4) == -1
+    assert call(V=4100) == -2          # V % 8
+    assert call(gamma=65) == -2
+    assert call(T_host=0) == -1
+    assert call(lens=0) == -1
+    assert call(T=0) == -1
+    assert call(ws=0) == -1
+    assert call(T_host=FAKE + 4) == -1  # misaligned
+    assert call(T=FAKE + 8) == -1
+    assert call(ws=FAKE + 16) == -1     # workspace not 256-aligned
+    assert call(R=0) == 0               # empty batch: nothing to do
