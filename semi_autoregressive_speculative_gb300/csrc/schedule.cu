@@ -27,6 +27,8 @@ constexpr int kSchedThreads = 1024;
 
 constexpr int kRadixDigits = 256;  // 8-bit digits, four passes over the upper 32 key bits
 constexpr int kSchedWarps = kSchedThreads / 32;
+// SPS entries that fit in the radix counts' shared memory (staged by cp.async)
+constexpr int kSpsStaged = (kSchedWarps + 8) * kRadixDigits * 4 / 8;
 
 // Stable LSD radix sort of b0[0, 1024 E) by key bits 32..63, ascending; b1 is
 // scratch of the same size and hist holds (32 + 8) x 256 ints.  Thread t =
@@ -37,7 +39,7 @@ constexpr int kSchedWarps = kSchedThreads / 32;
 // goes to its digit's base + the keys of that digit in earlier warps + its
 // rank in the warp.  On return b0 holds the sorted keys.
 template <int E>
-__device__ void radix_sort_keys(uint64_t* b0, uint64_t* b1, int* hist) {
+__device__ __noinline__ void radix_sort_keys(uint64_t* b0, uint64_t* b1, int* hist) {
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const unsigned below = (1u << lane) - 1u;
   int* gsum = hist + kSchedWarps * kRadixDigits;  // [4][256]: counts of warps 8g .. 8g+7
@@ -114,31 +116,36 @@ __device__ void radix_sort_keys(uint64_t* b0, uint64_t* b1, int* hist) {
   // four passes: the last one wrote b0
 }
 
-// Number of keys in v[b0, b1) (sorted ascending) that are below x.
-__device__ __forceinline__ int count_below(const uint64_t* v, int b0, int b1, uint64_t x) {
-  while (b0 < b1) {
-    const int m = (b0 + b1) >> 1;
-    if (v[m] < x) b0 = m + 1;
-    else b1 = m;
-  }
-  return b0;
-}
-
 // Sorts a[0, n) (distinct keys) whose runs [k run, (k + 1) run) are each
 // ascending, by merging adjacent runs level by level; b is scratch of the same
-// size.  On return a holds the sorted keys.
-__device__ void merge_sorted_runs(uint64_t* a, uint64_t* b, int n, int run) {
+// size.  On return a holds the sorted keys.  At every level thread t writes
+// the merged keys [E t, E t + E) (merge path): one binary search along the
+// diagonal finds how many of the first d keys of its merged run come from the
+// left run, then the thread merges its E keys in turn.
+__device__ void merge_sorted_runs(uint64_t* a, uint64_t* b, int n, int run, int E) {
   uint64_t* src = a;
   uint64_t* dst = b;
   for (int L = run; L < n; L <<= 1) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const uint64_t x = src[i];
-      const int lo = (i / (2 * L)) * (2 * L);
-      const int mid = min(lo + L, n), hi = min(lo + 2 * L, n);
-      // its index in its own run plus the keys of the partner run below it
-      const int pos = i < mid ? i + (count_below(src, mid, hi, x) - mid)
-                              : lo + (i - mid) + (count_below(src, lo, mid, x) - lo);
-      dst[pos] = x;
+    const int L2 = 2 * L;
+    int o = threadIdx.x * E;
+    const int oend = min(o + E, n);
+    while (o < oend) {
+      const int lo = (o / L2) * L2;
+      const int mid = min(lo + L, n), hi = min(lo + L2, n);
+      const int la = mid - lo, lb = hi - mid, d = o - lo;
+      // the smallest m with A[m] > B[d - m - 1]: keys of A among the first d
+      int x0 = max(0, d - lb), x1 = min(d, la);
+      while (x0 < x1) {
+        const int m = (x0 + x1) >> 1;
+        if (src[lo + m] < src[mid + d - m - 1]) x0 = m + 1;
+        else x1 = m;
+      }
+      int ia = x0, ib = d - x0;
+      const int stop = min(oend, hi);
+      for (; o < stop; ++o) {
+        const bool take_a = ia < la && (ib >= lb || src[lo + ia] < src[mid + ib]);
+        dst[o] = take_a ? src[lo + ia++] : src[mid + ib++];
+      }
     }
     __syncthreads();
     uint64_t* const tmp = src;
@@ -149,6 +156,39 @@ __device__ void merge_sorted_runs(uint64_t* a, uint64_t* b, int n, int run) {
     for (int i = threadIdx.x; i < n; i += blockDim.x) a[i] = src[i];
     __syncthreads();
   }
+}
+
+__device__ __forceinline__ void cp_async_8(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// round(v 2^40) to nearest, ties to even, for finite v >= 0, in integer
+// arithmetic (exactly the fp64 product rounded to int64: v 2^40 needs no more
+// than 24 significant bits); saturates at 2^63 - 1 from v >= 2^23 on.
+__device__ __forceinline__ int64_t q40(float v) {
+  const uint32_t bits = __float_as_uint(v);
+  const int e = static_cast<int>(bits >> 23);
+  if (e == 0) return 0;  // zero or subnormal: below 2^-86
+  const uint64_t mant = (bits & 0x7FFFFFu) | 0x800000u;  // v = mant 2^(e - 150)
+  const int sh = e - 110;                                 // v 2^40 = mant 2^sh
+  if (sh >= 0) return sh >= 40 ? INT64_MAX : static_cast<int64_t>(mant << sh);
+  const int s = -sh;
+  if (s > 24) return 0;  // below 1/2
+  const uint64_t q = mant >> s, rem = mant & ((1ull << s) - 1), half = 1ull << (s - 1);
+  return static_cast<int64_t>(q + ((rem > half || (rem == half && (q & 1))) ? 1 : 0));
+}
+
+// R + S 2^-40 in fp64, exactly, for S >= 0 and R 2^40 + S < 2^53: the sum
+// needs no rounding, so its double is built from the integer's bits (the fp64
+// pipe of GB300 is slow).
+__device__ __forceinline__ double tau_exact(int R, int64_t S) {
+  const int64_t T = (static_cast<int64_t>(R) << 40) + S;
+  const int p = 63 - __clzll(T);  // 40 <= p <= 52 (R >= 1)
+  const uint64_t bits = (static_cast<uint64_t>(p - 40 + 1023) << 52) |
+                        ((static_cast<uint64_t>(T) << (52 - p)) & ((1ull << 52) - 1));
+  return __longlong_as_double(static_cast<long long>(bits));
 }
 
 struct SchedSmem {
@@ -188,33 +228,40 @@ __global__ void __launch_bounds__(kSchedThreads)
   pdl_wait();
   const int n = R * gamma;
   const int tid = threadIdx.x;
-  // 1. keys, in (r, j) order: each request's run
+  // 1. keys, in (r, j) order: each request's run.  NaN, negative or infinite
+  // a is scheduled last (as 0) and reported; -0 is 0.
+  auto clean = [](float v) -> uint32_t {
+    return (!(v >= 0.f) || !(v <= 3.4e38f) || v == 0.f) ? 0u : __float_as_uint(v);
+  };
+  int rises = 0;  // some request's a rises along its positions
   for (int i = tid; i < npow2; i += kSchedThreads) {
     uint64_t key = ~0ull;
     if (i < n) {
-      float v = a[i];
-      if (!(v >= 0.f) || !(v <= 3.4e38f)) {  // NaN, negative or infinite: schedule it last
-        report(status, DSPARK_STATUS_NONFINITE);
-        v = 0.f;
-      }
-      const uint32_t bits = __float_as_uint(v);
+      const float v = a[i];
+      if (!(v >= 0.f) || !(v <= 3.4e38f)) report(status, DSPARK_STATUS_NONFINITE);
+      const uint32_t bits = clean(v);
       const int r = i / gamma, j = i - r * gamma;
+      if (j > 0 && clean(a[i - 1]) < bits) rises = 1;
       key = (static_cast<uint64_t>(0xFFFFFFFFu - bits) << 32) | (static_cast<uint64_t>(j) << 16) |
             static_cast<uint64_t>(r);
     }
     keys[i] = key;
   }
   for (int r = tid; r < R; r += kSchedThreads) cnt[r] = 0;
-  __syncthreads();
-  int rises = 0;  // some request's a rises along its positions
-  for (int i = tid; i < n; i += kSchedThreads)
-    if (i % gamma != 0 && keys[i] < keys[i - 1]) rises = 1;
   rises = __syncthreads_or(rises);
   // 2. sort, ascending key; the prefix-sum array is the scratch buffer
   {
     uint64_t* scratch = reinterpret_cast<uint64_t*>(S);
     if (!rises) {
-      merge_sorted_runs(keys, scratch, n, gamma);
+      merge_sorted_runs(keys, scratch, n, gamma, npow2 / kSchedThreads);
+      // the SPS entries of step 4 go to shared memory now, asynchronously, so
+      // that their latency hides behind steps 3 and the scan: into the radix
+      // counts' space, which the merge leaves unused (when they fit; otherwise
+      // step 4 reads them itself)
+      if (n + 1 <= kSpsStaged) {
+        for (int b = tid; b <= n; b += kSchedThreads) cp_async_8(reinterpret_cast<double*>(hist) + b, sps + R + b);
+        cp_async_commit();
+      }
     } else {
       // the keys in (j, r) order, the low key bits ascending, so that a stable
       // sort by the upper 32 bits is the full 64-bit order (npow2 = 1024 E,
@@ -238,7 +285,7 @@ __global__ void __launch_bounds__(kSchedThreads)
   for (int i = tid; i < n; i += kSchedThreads) {
     const uint64_t key = keys[i];
     const float v = __uint_as_float(0xFFFFFFFFu - static_cast<uint32_t>(key >> 32));
-    S[i + 1] = __double2ll_rn(static_cast<double>(v) * 0x1p40);
+    S[i + 1] = q40(v);
     rid[i] = static_cast<uint16_t>(key & 0xFFFFu);
   }
   if (tid == 0) S[0] = 0;
@@ -272,11 +319,18 @@ __global__ void __launch_bounds__(kSchedThreads)
     const int64_t offset = (x - run) + (wid > 0 ? s_warp[wid - 1] : 0);
     for (int i = lo; i < hi; ++i) S[i] += offset;
   }
+  const bool staged = !rises && n + 1 <= kSpsStaged;  // SPS(R + b) in shared memory
+  if (staged) cp_async_wait_all();
   __syncthreads();
   // 4. Theta(b) (overwrites the key storage; rid keeps what is still needed)
-  for (int b = tid; b <= n; b += kSchedThreads) {
-    const double tau = __dadd_rn(static_cast<double>(R), static_cast<double>(S[b]) * 0x1p-40);
-    th[b] = __dmul_rn(tau, sps[R + b]);
+  // S_b never falls as b grows (Q.40 values are >= 0; a sum that overflowed
+  // is negative), so S_n decides for every b whether tau is exact
+  if (S[n] >= 0 && (static_cast<int64_t>(R) << 40) + S[n] < (1ll << 53)) {
+    for (int b = tid; b <= n; b += kSchedThreads)
+      th[b] = __dmul_rn(tau_exact(R, S[b]), staged ? reinterpret_cast<const double*>(hist)[b] : sps[R + b]);
+  } else {
+    for (int b = tid; b <= n; b += kSchedThreads)
+      th[b] = __dmul_rn(__dadd_rn(static_cast<double>(R), static_cast<double>(S[b]) * 0x1p-40), sps[R + b]);
   }
   __syncthreads();
   // first descent (early stop) and global argmax (lowest b on ties).  The

@@ -133,6 +133,33 @@ def test_schedule_rows_that_rise(R, gamma, seed):
         _assert_same(got, exp)
 
 
+@pytest.mark.parametrize("case", ["zeros_and_halves", "large_values"])
+def test_schedule_edge_values(case):
+    """Values that exercise the fixed-point and Theta arithmetic, against the
+    oracle bit for bit: signed zeros (-0 ties with 0, broken by (j, r)),
+    subnormals (round to 0 in Q.40), values whose Q.40 image is an exact half
+    (ties to even), and a above 1 (not survival products, but admissible) large
+    enough that R + S_b no longer fits 53 bits."""
+    from semi_autoregressive_speculative_gb300.round import DeviceRound
+    rng = np.random.default_rng(21)
+    R, gamma = 33, 7
+    if case == "zeros_and_halves":
+        # descending; in Q.40: 1.5 -> 2, 1.25 -> 1, 0.5 -> 0, 0.25 -> 0, a subnormal -> 0
+        pool = np.array([0.75, 0.5, 3 * 2.0 ** -41, 5 * 2.0 ** -42, 2.0 ** -41, 2.0 ** -42, 1e-45, 0.0, -0.0],
+                        dtype=np.float32)
+        # each request a non-increasing run drawn from the pool (-0 and 0 compare equal)
+        a = np.stack([pool[np.sort(rng.integers(0, len(pool), gamma))] for _ in range(R)])
+    else:
+        a = np.sort(rng.uniform(1.0, 4.0e6, (R, gamma)), axis=1)[:, ::-1].astype(np.float32)
+        assert float(a.astype(np.float64).sum()) > 2.0 ** 13  # R 2^40 + S_n above 2^53
+    dr = DeviceRound(R, gamma, 64, 64, 8)
+    B = np.arange(R * (1 + gamma) + 1, dtype=np.float64)
+    sps = 1.0 / np.maximum(1.0, B / (R * 3.0))
+    for mode, K in [(0, 0), (1, R * gamma // 2), (2, 0)]:
+        got, exp = _schedule_both(dr, a, sps, mode, K)
+        _assert_same(got, exp)
+
+
 def test_schedule_handbook_planner_inputs():
     # the page's adaptive-planner confidences, batch 512 x 7, against the oracle
     torch_ = pytest.importorskip("torch")
