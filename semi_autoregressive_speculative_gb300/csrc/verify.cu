@@ -9,7 +9,8 @@
 //                   partials of T / temperature (or max / argmax), and the
 //                   target logit at the drafted token.
 //  k4_accept        one CTA per request: per row max and normaliser, the
-//                   accept test u < p_t(x) / p_d(x) position by position, the
+//                   accept tests u < p_t(x) / p_d(x) of all positions at once
+//                   (the first rejection is the lowest rejected position), the
 //                   bonus draw from row lens[r] when everything is accepted,
 //                   otherwise the request joins the rejection list.
 //  k_residual_partials  tensor-core recompute of the draft rows at the
@@ -241,18 +242,30 @@ __device__ int sample_target_row(const VerifyArgs& p, size_t trw, float M, float
 }
 
 // One CTA per request: warp w computes the statistics of rows w, w+8, ...;
-// the accept tests then run in position order.
+// then thread j runs the accept test of position j (all at once: the tests
+// are independent, and the first rejection is the lowest rejected j).
 __global__ void __launch_bounds__(256) k4_accept(const VerifyArgs p) {
   __shared__ BlockFindScratch sc;
-  __shared__ float s_M[kMaxGamma + 1], s_Z[kMaxGamma + 1];
+  __shared__ float s_M[kMaxGamma + 1], s_Z[kMaxGamma + 1], s_tz[kMaxGamma + 1];
   __shared__ int s_am[kMaxGamma + 1];
-  __shared__ int s_n;
+  __shared__ unsigned s_rej[2];  // rejected positions 0..31 and 32..63
   pdl_launch_dependents();
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int r = blockIdx.x;
   const int len = clamp_len(p.lens[r], p.gamma, nullptr);
   const size_t base_row = static_cast<size_t>(r) * (p.gamma + 1);
+  // the accept test's own inputs (thread j < len: position j), read and drawn
+  // before the row statistics
+  int tok = 0;
+  float pd = 0.f, u = 0.f;
+  if (tid < len) {
+    tok = p.tokens[static_cast<size_t>(r) * p.gamma + tid];
+    if (!p.greedy) {
+      pd = p.pd_tok[static_cast<size_t>(r) * p.gamma + tid];
+      u = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(tid), kAcceptTest);
+    }
+  }
   for (int j = wid; j <= len; j += 8) {
     const float2* st = p.tstats + (base_row + j) * p.n_vc;
     if (p.greedy) {
@@ -262,39 +275,36 @@ __global__ void __launch_bounds__(256) k4_accept(const VerifyArgs p) {
       float M, Z;
       row_stats(st, p.n_vc, &M, &Z);
       if (lane == 0) {
+        const float tz = p.trow[base_row + j].z;
         s_M[j] = M;
         s_Z[j] = Z;
-        p.trow[base_row + j] = make_float4(M, Z, p.trow[base_row + j].z, 0.f);
+        s_tz[j] = tz;
+        p.trow[base_row + j] = make_float4(M, Z, tz, 0.f);
       }
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    int n = len;
-    for (int j = 0; j < len; ++j) {
-      bool accept;
-      if (p.greedy) {
-        accept = p.tokens[static_cast<size_t>(r) * p.gamma + j] == s_am[j];
+  bool rejected = false, nonfinite = false;
+  if (tid < len) {
+    if (p.greedy) {
+      rejected = tok != s_am[tid];
+    } else {
+      const float M = s_M[tid], Z = s_Z[tid];
+      if (!(fabsf(M) <= 3.4e38f) || !(Z > 0.f) || !(Z <= 3.4e38f)) {
+        rejected = nonfinite = true;
       } else {
-        const float M = s_M[j], Z = s_Z[j];
-        if (!(fabsf(M) <= 3.4e38f) || !(Z > 0.f) || !(Z <= 3.4e38f)) {
-          report(p.status, DSPARK_STATUS_NONFINITE);
-          accept = false;
-        } else {
-          const float pt = exp2f(p.trow[base_row + j].z * p.scale - M) / Z;
-          const float pd = p.pd_tok[static_cast<size_t>(r) * p.gamma + j];
-          const float u = uniform24(p.seed, p.round, static_cast<uint64_t>(r), static_cast<uint64_t>(j), kAcceptTest);
-          // accept iff u < p_t / p_d, evaluated as u * p_d < p_t (p_d > 0)
-          accept = !(pd > 0.f) || u * pd < pt;
-        }
+        const float pt = exp2f(s_tz[tid] * p.scale - M) / Z;
+        // accept iff u < p_t / p_d, evaluated as u * p_d < p_t (p_d > 0)
+        rejected = !(!(pd > 0.f) || u * pd < pt);
       }
-      if (!accept) { n = j; break; }
     }
-    s_n = n;
-    p.n_accept[r] = n;
   }
+  const unsigned rej_bits = __ballot_sync(0xffffffffu, rejected);
+  if (wid < 2 && lane == 0) s_rej[wid] = rej_bits;
   __syncthreads();
-  const int n = s_n;
+  const int n = s_rej[0] ? __ffs(s_rej[0]) - 1 : s_rej[1] ? 32 + __ffs(s_rej[1]) - 1 : len;
+  if (tid == n && nonfinite) report(p.status, DSPARK_STATUS_NONFINITE);  // the first rejection's row
+  if (tid == 0) p.n_accept[r] = n;
   if (p.greedy) {
     if (tid == 0) {
       const int nxt = s_am[n];
@@ -394,9 +404,15 @@ __global__ void __launch_bounds__(256) k4_residual_sample(const __grid_constant_
   const int prev_raw = n == 0 ? p.anchors[r] : p.tokens[static_cast<size_t>(r) * p.gamma + n - 1];
   const int prev = (prev_raw >= 0 && prev_raw < p.V) ? prev_raw : 0;
   for (int k = tid; k < p.rank; k += 256) s_e[k] = bf16_at(p.W1 + static_cast<size_t>(prev) * p.rank + k);
+  // the sub-tile's U and T values, read while the slab is in flight
+  const int v = v0 + lane;
+  float u_v = 0.f, t_v = 0.f;
+  if (wid == 0 && v < p.V) {
+    u_v = p.U[(static_cast<size_t>(r) * p.gamma + n) * p.V + v];
+    t_v = p.T[trw * p.V + v];
+  }
   if (tid == 0) s_landed = mbar_wait(bar, 0, &s_no_abort) ? 1 : 0;  // bounded; one waiter, shared verdict
   __syncthreads();
-  const int v = v0 + lane;
   float acc = 0.f;
   if (s_landed) {
 #pragma unroll 8
@@ -416,8 +432,8 @@ __global__ void __launch_bounds__(256) k4_residual_sample(const __grid_constant_
 #pragma unroll
       for (int k = 0; k < 8; ++k) b += s_part[k][lane];
       const float l2zd = p.logZd[static_cast<size_t>(r) * p.gamma + n] * 1.4426950408889634f;
-      const float pd = exp2f((b + p.U[(static_cast<size_t>(r) * p.gamma + n) * p.V + v]) * p.scale - l2zd);
-      const float pt = exp2f(p.T[trw * p.V + v] * p.scale - Mt) / Zt;
+      const float pd = exp2f((b + u_v) * p.scale - l2zd);
+      const float pt = exp2f(t_v * p.scale - Mt) / Zt;
       w = fmaxf(pt - pd, 0.f);
     }
     const float incl = before_s + warp_incl_scan_f(w);
