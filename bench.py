@@ -42,7 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per dspark_markov_draft call (one round's 16 positions) from the
 # ncu capture summarised in profiles/; valid only for the draft kernel sources
 # whose digest (draft_digest) is recorded with it.
-NCU_DRAFT_TRAFFIC = {"digest": "0162e3e014ab", "workload": "r128_g16_v151936", "bytes_per_call": 1378331136 + 16611584}
+NCU_DRAFT_TRAFFIC = {"digest": "d020ed141c19", "workload": "r128_g16_v151936", "bytes_per_call": 1377694720 + 17224192}
 
 
 # ----------------------------------------------------------------------------- helpers
