@@ -5,15 +5,16 @@
 //      sorted.  Survival products never rise along a request (each step
 //      multiplies by a confidence <= 1, and fp32 rounding is monotone), so
 //      each request's keys already form a sorted run and the order is a merge
-//      of R runs: ceil(log2 R) levels in which every key finds its place by a
-//      binary search of the partner run.  The keys are distinct, so this is
-//      exactly the sorted order.  Rows that do rise (a caller's own a, or
-//      values reported as non-finite) take the general path: a stable radix
-//      sort of the keys written in (j, r) order on their upper 32 bits (four
-//      8-bit passes);
-//   2. a -> Q.40 fixed point and an integer inclusive scan: S_b is the same for
-//      every summation order;
-//   3. Theta(b) = (R + S_b 2^-40) * SPS[R + b] in fp64 for every b;
+//      of R runs: ceil(log2 R) levels, each a merge path (one diagonal search
+//      per thread, then a sequential merge of its keys).  The keys are
+//      distinct, so this is exactly the sorted order.  Rows that do rise (a
+//      caller's own a, or values reported as non-finite) take the general
+//      path: a stable radix sort of the keys written in (j, r) order on their
+//      upper 32 bits (four 8-bit passes);
+//   2. a -> Q.40 fixed point (an exact integer rounding) and an integer
+//      inclusive scan: S_b is the same for every summation order;
+//   3. Theta(b) = (R + S_b 2^-40) * SPS[R + b] in fp64 for every b (the sum
+//      built exactly from integer bits when it fits 53 bits);
 //   4. b* by mode (first descent / min(K, n) / n) and the global argmax;
 //   5. lens[r] = admitted pairs of request r.
 #include <cmath>
