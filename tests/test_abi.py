@@ -138,3 +138,12 @@ def test_load_rows_validation(L):
     assert call(T=FAKE + 8) == -1
     assert call(ws=FAKE + 16) == -1     # workspace not 256-aligned
     assert call(R=0) == 0               # empty batch: nothing to do
+
+
+def test_load_rows_binding_checks_the_host_shape():
+    # the binding's own shape check runs before the library is called
+    import torch
+    import semi_autoregressive_speculative_gb300 as pkg
+    T = torch.empty((3, 5, 16))
+    with pytest.raises(ValueError):
+        pkg.dspark_load_verified_rows(torch.empty((3, 4, 16)), None, T, None)
