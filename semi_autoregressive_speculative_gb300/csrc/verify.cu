@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(256) k4_residual_sample(const __grid_constant_
     u_v = p.U[(static_cast<size_t>(r) * p.gamma + n) * p.V + v];
     t_v = p.T[trw * p.V + v];
   }
-  if (tid == 0) s_landed = mbar_wait(bar, 0, &s_no_abort) ? 1 : 0;  // bounded; one waiter, shared verdict
+  if (tid == 0) s_landed = mbar_wait(bar, 0, &s_no_abort) ? 1 : 0;  // bounded; one waiter, result shared
   __syncthreads();
   float acc = 0.f;
   if (s_landed) {
